@@ -1,0 +1,226 @@
+"""Exact-attention oracle: plain, slow, obviously correct CPU references.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg (and its ``--impl reference`` arm) may import this
+package.  It shares no code with the CUDA path and never calls it; the CUDA
+path never calls it either.
+
+Three independent references, each in fp64 or better:
+
+``attention``          the plain definition ("6.1 FlashAttention V1 in detail",
+                       section 1.1: S = scale * Q K^T, P = softmax(S), O = P V)
+                       with the softmax written as the three-pass safe softmax of
+                       section 3.1 and LSE = m + log(l) ("FlashAttention:
+                       IO-Aware Tiling, ...", section "Backward Pass
+                       Recomputation").  Compiled C (``attn_oracle.c``), OpenMP
+                       over rows, so that full-size rows stay affordable.
+``attention_online``   the tile-by-tile (m, l, u) merge of "FlashAttention:
+                       optimize data movement before counting FLOPs", section 02
+                       (m' = max(m, max s); l' = e^(m-m') l + sum e^(s-m');
+                       u' = e^(m-m') u + sum e^(s-m') V; output u'/l'), in numpy
+                       fp64, with any tile sizes and any K/V-tile visiting order.
+                       It exists to pin the online reasoning, not the GPU.
+``attention_decimal``  brute force in Python ``decimal`` at 50 digits, using
+                       the softmax definition directly (exp(s_j) / sum exp(s_k),
+                       no max shift) - an independent formulation for tiny
+                       inputs.
+
+Readings where the pages are silent (shared by all three):
+  * ``scale`` is applied exactly as given (the configs use 1/sqrt(d), passed
+    as the fp32 value the GPU receives);
+  * causal keeps keys j <= i for query row i (N_q = N_k);
+  * the log is natural, over the scaled logits.
+
+Every function here is pinned by ``tests/test_oracle.py`` against values the
+pages print, closed forms, invariants and brute force.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from decimal import Decimal, getcontext
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``attn_oracle.c`` into ``_build/liboracle.so`` (gcc, -O2, OpenMP
+    when available, never -ffast-math).  Returns the library path."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    base = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-fno-fast-math",
+            "-ffp-contract=off", _SRC, "-o", _LIB_PATH + ".tmp", "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(_LIB_PATH + ".tmp", _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        lib.oracle_attention_rows.restype = ctypes.c_int
+        lib.oracle_attention_rows.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_double, ctypes.c_int,
+            ctypes.c_void_p, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_max_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def max_threads() -> int:
+    """Threads the compiled oracle uses by default."""
+    return int(_load().oracle_max_threads())
+
+
+def _bf16_bits(t) -> np.ndarray:
+    """bf16 torch tensor (CPU) -> contiguous uint16 numpy view of its bits."""
+    import torch
+    if t.dtype != torch.bfloat16:
+        raise TypeError("oracle inputs are bf16 tensors")
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _as_f64(t) -> np.ndarray:
+    """bf16 torch tensor -> float64 numpy array (exact widening)."""
+    import torch
+    return t.detach().cpu().to(torch.float64).numpy()
+
+
+def attention(q, k, v, scale: float, causal: bool, rows=None, threads: int = 0):
+    """fp64 attention of bf16 inputs by the plain definition.
+
+    q, k, v : bf16 CPU tensors [B, H, N, d]
+    rows    : None (all rows) or an int64 array of flat row ids
+              (b*H + h)*N + i
+    Returns (O, LSE) as float64 numpy arrays: [B, H, N, d] and [B, H, N] for
+    all rows, else [len(rows), d] and [len(rows)].
+    """
+    B, H, N, d = q.shape
+    if tuple(k.shape) != (B, H, N, d) or tuple(v.shape) != (B, H, N, d):
+        raise ValueError("q, k, v must share the shape [B, H, N, d]")
+    qb, kb, vb = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v)
+    if rows is None:
+        n_rows = B * H * N
+        rows_arr = None
+        rows_ptr = None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        n_rows = rows_arr.size
+        rows_ptr = rows_arr.ctypes.data
+    o = np.empty((n_rows, d), dtype=np.float64)
+    lse = np.empty((n_rows,), dtype=np.float64)
+    rc = _load().oracle_attention_rows(
+        qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, B, H, N, d,
+        float(scale), int(bool(causal)), rows_ptr, n_rows,
+        o.ctypes.data, lse.ctypes.data, int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_rows failed ({rc})")
+    if rows is None:
+        return o.reshape(B, H, N, d), lse.reshape(B, H, N)
+    return o, lse
+
+
+def attention_online(q, k, v, scale: float, causal: bool, block_q: int,
+                     block_k: int, order=None, mask_tail: bool = True):
+    """Tile-by-tile online softmax with the (m, l, u) merge, fp64 numpy.
+
+    Q is cut into tiles of ``block_q`` rows and K/V into tiles of ``block_k``
+    rows (the last tiles may be partial); each Q tile visits the K/V tiles in
+    ``order`` (a permutation of range(T_c); default ascending).  Per visit:
+        s  = scale * Q_i K_j^T       (columns past N, and causal j > i, -> -inf)
+        m' = max(m, rowmax s)
+        l' = exp(m - m') l + rowsum exp(s - m')
+        u' = exp(m - m') u + exp(s - m') V_j
+    and finally O = u / l, LSE = m + log l.  A row whose m' is still -inf (every
+    key seen so far masked) keeps m = -inf, l = 0, u = 0.
+
+    ``mask_tail=False`` pads the last K/V tile with zero rows and lets their
+    scores (0) into the softmax - the mistake the K/V out-of-range mask exists
+    to prevent ("6.1 FlashAttention V1 in detail", section 8.3).  It is here
+    only so a test can show that the mistake is caught.
+    """
+    qd, kd, vd = _as_f64(q), _as_f64(k), _as_f64(v)
+    B, H, N, d = qd.shape
+    t_c = -(-N // block_k)
+    if order is None:
+        order = range(t_c)
+    order = list(order)
+    if sorted(order) != list(range(t_c)):
+        raise ValueError("order must be a permutation of the K/V tiles")
+    pad = t_c * block_k - N
+    kp = np.concatenate([kd, np.zeros((B, H, pad, d))], axis=2) if pad else kd
+    vp = np.concatenate([vd, np.zeros((B, H, pad, d))], axis=2) if pad else vd
+    o = np.empty((B, H, N, d))
+    lse = np.empty((B, H, N))
+    for i0 in range(0, N, block_q):
+        i1 = min(i0 + block_q, N)
+        qi = qd[:, :, i0:i1, :]
+        rows = np.arange(i0, i1)
+        m = np.full((B, H, i1 - i0), -np.inf)
+        l = np.zeros((B, H, i1 - i0))
+        u = np.zeros((B, H, i1 - i0, d))
+        for j in order:
+            j0, j1 = j * block_k, (j + 1) * block_k
+            s = scale * np.einsum("bhic,bhjc->bhij", qi, kp[:, :, j0:j1, :])
+            cols = np.arange(j0, j1)
+            if mask_tail:
+                s[..., cols >= N] = -np.inf
+            if causal:
+                s[..., cols[None, :] > rows[:, None]] = -np.inf
+            m_new = np.maximum(m, s.max(axis=-1))
+            live = np.isfinite(m_new)
+            ref = np.where(live, m_new, 0.0)
+            alpha = np.where(live, np.exp(m - ref), 1.0)
+            p = np.exp(s - ref[..., None])
+            l = alpha * l + p.sum(axis=-1)
+            u = alpha[..., None] * u + np.einsum("bhij,bhjc->bhic", p, vp[:, :, j0:j1, :])
+            m = m_new
+        o[:, :, i0:i1, :] = u / l[..., None]
+        lse[:, :, i0:i1] = m + np.log(l)
+    return o, lse
+
+
+def attention_decimal(q, k, v, scale, causal: bool, digits: int = 50):
+    """Brute force in ``decimal``: softmax by its definition, no max shift.
+
+    P_ij = exp(s_ij) / sum_k exp(s_ik) over admitted keys; O_i = sum_j P_ij V_j;
+    LSE_i = ln(sum_k exp(s_ik)).  For tiny inputs only (pure Python loops).
+    Returns nested lists of Decimal: O [B][H][N][d], LSE [B][H][N].
+    """
+    getcontext().prec = digits
+    qd, kd, vd = _as_f64(q), _as_f64(k), _as_f64(v)
+    B, H, N, d = qd.shape
+    sc = Decimal(float(scale))
+    O = [[[[None] * d for _ in range(N)] for _ in range(H)] for _ in range(B)]
+    L = [[[None] * N for _ in range(H)] for _ in range(B)]
+    for b in range(B):
+        for h in range(H):
+            for i in range(N):
+                keys = range(i + 1) if causal else range(N)
+                e = {}
+                for j in keys:
+                    dot = sum(Decimal(float(qd[b, h, i, c])) * Decimal(float(kd[b, h, j, c]))
+                              for c in range(d))
+                    e[j] = (sc * dot).exp()
+                z = sum(e.values())
+                for c in range(d):
+                    O[b][h][i][c] = sum(e[j] * Decimal(float(vd[b, h, j, c])) for j in keys) / z
+                L[b][h][i] = z.ln()
+    return O, L
