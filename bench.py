@@ -1,0 +1,405 @@
+#!/usr/bin/env python
+"""Benchmark: fused exact attention forward on GB300, one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one forward pass (one fa_fwd launch) over the whole workload, with
+inputs resident in device memory.  The default workload is the long causal
+run B=1, H=32, N=16384, d=128.  Q/K/V (402 MB) plus O (134 MB) exceed the
+129 MB L2, so consecutive steps do not run from a warm L2.
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(independent replicas, weak scaling; no collective touches the data; a barrier
+and a max-reduce of the timings only).
+
+``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample of
+rows of the same workload, and reports the same metric for it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_attention_32_gb300.workloads import HEADLINE, WORKLOADS, workload_inputs  # noqa: E402
+
+METRIC = "attention fwd TFLOPS (bf16, 1×GB300) and % of dense BF16 tensor peak"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+KERNEL_SOURCES = {"fa_fwd_mma_kernel": "exact_attention_32_gb300/csrc/fa_fwd_mma.cu"}
+DOMINANT_KERNEL = "fa_fwd_mma_kernel"
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--cpu-seconds", type=float, default=15.0,
+                   help="target CPU time of the oracle baseline sample")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------- distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------- peaks
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(kernel: str, workload: str):
+    """dram read+write bytes per launch from the committed ncu summary of this
+    kernel and workload, or None when absent or taken on a different source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    src = os.path.join(ROOT, KERNEL_SOURCES[kernel])
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    m_t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_s = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    if not m_t or not m_s or m_s.group(1) != sha:
+        return None
+    return float(m_t.group(1))
+
+
+# --------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, every 100 ms."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.file = None
+        self.target = None
+        try:
+            props = torch.cuda.get_device_properties(device_index)
+            self.target = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else None
+        except Exception:
+            self.target = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                   "-lms", "100"]
+            if self.target:
+                cmd += ["-i", self.target]
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [line.strip().split(",") for line in self.file if line.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- CPU baseline
+
+def oracle_rows_for(w, seconds: float, threads: int, rng_seed: int = 0):
+    """Evenly spaced rows of the workload whose fp64 oracle cost is about
+    ``seconds`` on ``threads`` threads (calibrated on a small first batch)."""
+    import oracle
+    q, k, v = workload_inputs(w)
+    total = w.B * w.H * w.N
+    n = max(threads * 2, 8)
+    while True:
+        calib = np.linspace(0, total - 1, min(n, total)).round().astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, w.scale, w.causal, rows=calib, threads=threads)
+        dt = time.perf_counter() - t0
+        if dt >= min(0.5, seconds / 4) or n >= total:
+            break
+        n *= 4
+    per_row = dt / len(calib)
+    n = int(min(total, max(len(calib), seconds / max(per_row, 1e-9))))
+    rows = np.unique(np.linspace(0, total - 1, n).round().astype(np.int64))
+    return (q, k, v), rows
+
+
+def time_oracle(w, inputs, rows, threads):
+    import oracle
+    q, k, v = inputs
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, w.scale, w.causal, rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    # conventional work of those rows: the workload's FLOPs spread evenly over its rows
+    flops = w.flops * len(rows) / (w.B * w.H * w.N)
+    return dt, flops
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, seconds):
+    threads = cpu_threads()
+    inputs, rows = oracle_rows_for(w, seconds, threads)
+    dt, flops = time_oracle(w, inputs, rows, threads)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(rows)} evenly spaced query rows of {w.B * w.H * w.N} "
+                      f"({w.name}), fp64 C oracle, {dt:.1f} s"}
+
+
+# ------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local):
+    import exact_attention_32_gb300 as fa
+
+    w = WORKLOADS[args.workload]
+    dev = torch.device("cuda", local if world > 1 else 0)
+    fa.lib()
+    q_h, k_h, v_h = workload_inputs(w)
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr())
+
+    def step():
+        st = fa.fa_fwd(*ptrs, w.B, w.H, w.N, w.d, w.scale, w.causal, sp)
+        if st != 0:
+            raise fa.FAError(st, "fa_fwd")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = fa.fa_get_device_status(sp)
+    if st != 0:
+        raise fa.FAError(st, "warm-up")
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    e0.record(stream)
+    for i in range(K):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    st = fa.fa_get_device_status(sp)
+    if st != 0:
+        raise fa.FAError(st, "timed region")
+    total_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    launch_ms = max_over_ranks(launch_ms, world)
+
+    value = w.flops * K * world / (total_ms / 1e3) / 1e12
+
+    # end to end through the public API: pinned host inputs in, O and LSE out
+    e2e = None
+    if not args.no_e2e:
+        qp, kp, vp_ = (t.pin_memory() for t in (q_h, k_h, v_h))
+        op = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        lp = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+        def e2e_step():
+            q.copy_(qp, non_blocking=True)
+            k.copy_(kp, non_blocking=True)
+            v.copy_(vp_, non_blocking=True)
+            fa.forward(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse)
+            op.copy_(o, non_blocking=True)
+            lp.copy_(lse, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        Ke = max(3, min(K, 30))
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+        in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
+        out_bytes = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+        e2e = {"value": w.flops * Ke * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
+               "steps": Ke, "ms_per_step": e2e_ms / Ke}
+
+    if rank != 0:
+        return None
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = w.flops / (launch_ms / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: Q, K, V iid N(0,1) fp32 rounded to bf16, seeded",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "scale": w.scale, "global_batch": w.B * world,
+                   "seq_len": w.N, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (Q+K+V+O exceed 129 MB), no flush"},
+        "pct_of_dense_bf16_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "tensor", "kernel": DOMINANT_KERNEL, "achieved": achieved,
+                     "peak": peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "unit": "TFLOP/s", "frac": achieved / peak,
+                     "traffic": load_traffic(DOMINANT_KERNEL, w.name),
+                     "algorithmic_flops_per_launch": w.flops,
+                     "algorithmic_bytes_per_launch": w.min_bytes,
+                     "launch_ms": launch_ms},
+        "gpu_launches": K,
+        "impl": "ours",
+    }
+    if e2e:
+        line["e2e"] = e2e
+    line["clocks"] = clk
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    return line
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = WORKLOADS[args.workload]
+    threads = cpu_threads()
+    budget = 150.0  # seconds of oracle work for the whole run
+    per_step = budget / max(1, args.steps + args.warmup)
+    inputs, rows = oracle_rows_for(w, per_step, threads)
+    for _ in range(args.warmup):
+        time_oracle(w, inputs, rows, threads)
+    total, flops = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, f = time_oracle(w, inputs, rows, threads)
+        total += dt
+        flops += f
+    value = flops / total / 1e12
+    return {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: Q, K, V iid N(0,1) fp32 rounded to bf16, seeded",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "seq_len": w.N, "parallelism": "host cores"},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{len(rows)} evenly spaced query rows per step of "
+                                   f"{w.B * w.H * w.N} ({w.name}), fp64 C oracle"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup(args)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,111 @@
+"""ctypes binding of libfa.so: argument marshalling only.
+
+Every function of include/fa.h is exposed under the same name; ``forward`` is
+the tensor-level convenience call.  Torch supplies device memory and the
+current stream; all arithmetic runs in the library's CUDA kernels.  There is
+no fallback: if libfa.so is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa.so")
+_lib = None
+_lock = threading.Lock()
+
+FA_OK = 0
+STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_NO_DEVICE",
+                4: "FA_ERR_ARCH", 5: "FA_ERR_LAUNCH", 6: "FA_ERR_TIMEOUT"}
+EXPORTED = ("fa_fwd", "fa_get_device_status", "fa_status_string", "fa_version")
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fa_status_string(status)}")
+
+
+def lib():
+    """Load libfa.so (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "exact_attention_32_gb300.build.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i64 = ctypes.c_void_p, ctypes.c_int64
+            L.fa_fwd.restype = ctypes.c_int
+            L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
+                                 ctypes.c_int, vp]
+            L.fa_get_device_status.restype = ctypes.c_int
+            L.fa_get_device_status.argtypes = [vp]
+            L.fa_status_string.restype = ctypes.c_char_p
+            L.fa_status_string.argtypes = [ctypes.c_int]
+            L.fa_version.restype = ctypes.c_int
+            L.fa_version.argtypes = []
+            _lib = L
+    return _lib
+
+
+def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
+    """Raw call: pointers as ints, ``stream`` a cudaStream_t as int (0 = legacy default)."""
+    return lib().fa_fwd(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), int(causal), stream)
+
+
+def fa_get_device_status(stream=0) -> int:
+    return lib().fa_get_device_status(stream)
+
+
+def fa_status_string(status: int) -> str:
+    return lib().fa_status_string(int(status)).decode()
+
+
+def fa_version() -> int:
+    return lib().fa_version()
+
+
+def default_scale(d: int) -> float:
+    """fp32 value of 1/sqrt(d) as a Python float."""
+    return float(np.float32(1.0 / math.sqrt(d)))
+
+
+def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
+            causal: bool = False, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+            stream: torch.cuda.Stream | None = None):
+    """O, LSE = attention(q, k, v) on the GPU through ``fa_fwd``.
+
+    q, k, v: bf16 CUDA tensors [B, H, N, d], contiguous.  Returns (O bf16
+    [B, H, N, d], LSE fp32 [B, H, N]); ``out``/``lse`` may be given to write
+    in place.  Enqueued on ``stream`` (default: torch's current stream).
+    """
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must all be [B, H, N, d]")
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = default_scale(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B, H, N]")
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                    B, H, N, d, float(scale), bool(causal), s.cuda_stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd")
+    return out, lse

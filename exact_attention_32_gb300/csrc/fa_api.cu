@@ -1,0 +1,137 @@
+// C ABI of libfa.so: argument validation, device checks and kernel dispatch.
+// The operation and every argument are documented in include/fa.h.
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool checked = false;
+    int status = FA_OK;  // FA_OK or FA_ERR_ARCH
+    int sm_count = 0;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_devices_mu;
+
+int current_device(int *dev, int *sm_count)
+{
+    if (cudaGetDevice(dev) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_NO_DEVICE;
+    }
+    if (*dev < 0 || *dev >= kMaxDevices) return FA_ERR_NO_DEVICE;
+    std::lock_guard<std::mutex> lock(g_devices_mu);
+    DeviceInfo &info = g_devices[*dev];
+    if (!info.checked) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess) {
+            cudaGetLastError();
+            return FA_ERR_NO_DEVICE;
+        }
+        info.status = (major == 10 && minor == 3) ? FA_OK : FA_ERR_ARCH;
+        info.sm_count = sms;
+        info.checked = true;
+    }
+    *sm_count = info.sm_count;
+    return info.status;
+}
+
+// A pointer the kernels may dereference: 16-byte aligned device (or managed)
+// memory of the current device.
+int check_pointer(const void *p, int dev)
+{
+    if (p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) != 0) return FA_ERR_INVALID_ARG;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_INVALID_ARG;
+    }
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return FA_ERR_INVALID_ARG;
+    if (a.device != dev) return FA_ERR_NO_DEVICE;
+    return FA_OK;
+}
+
+bool overlaps(const void *a, uint64_t na, const void *b, uint64_t nb)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+}  // namespace
+
+extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                      int64_t H, int64_t N, int64_t d, float scale, int causal, void *stream)
+{
+    // sizes first: nothing is touched for an invalid problem
+    if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (N > (int64_t(1) << 31) - 256 || B > (int64_t(1) << 31) || H > (int64_t(1) << 31))
+        return FA_ERR_INVALID_ARG;
+    if (B * H > (int64_t(1) << 40) / N || B * H * N > (int64_t(1) << 40) / d) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+
+    int dev = 0, sm_count = 0;
+    int st = current_device(&dev, &sm_count);
+    if (st != FA_OK) return st;
+    const void *ptrs[5] = {q, k, v, o, lse};
+    for (const void *p : ptrs)
+        if ((st = check_pointer(p, dev)) != FA_OK) return st;
+
+    const uint64_t tbytes = static_cast<uint64_t>(B * H * N * d) * 2u;
+    const uint64_t lbytes = static_cast<uint64_t>(B * H * N) * 4u;
+    if (overlaps(o, tbytes, lse, lbytes)) return FA_ERR_INVALID_ARG;
+    for (const void *in : {q, k, v})
+        if (overlaps(o, tbytes, in, tbytes) || overlaps(lse, lbytes, in, tbytes)) return FA_ERR_INVALID_ARG;
+
+    FaProblem p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.lse = lse;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.d = static_cast<int>(d);
+    p.scale = scale;
+    p.causal = causal;
+    p.sm_count = sm_count;
+    const cudaError_t e = fa_launch_mma(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return FA_ERR_LAUNCH;
+    return FA_OK;
+}
+
+extern "C" int fa_get_device_status(void *stream)
+{
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_LAUNCH;
+    }
+    return FA_OK;
+}
+
+extern "C" const char *fa_status_string(int status)
+{
+    switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dimension must be 64 or 128";
+    case FA_ERR_NO_DEVICE: return "FA_ERR_NO_DEVICE: no CUDA device, or pointer on another device";
+    case FA_ERR_ARCH: return "FA_ERR_ARCH: device is not compute capability 10.3 (sm_103)";
+    case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH: CUDA launch or execution error";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a bounded in-kernel wait gave up";
+    default: return "unknown fa_status";
+    }
+}
+
+extern "C" int fa_version(void) { return 100; }

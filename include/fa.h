@@ -1,0 +1,95 @@
+/*
+ * fa.h - C ABI of the GB300 (sm_103a) exact attention forward library (libfa.so).
+ *
+ * The operation is scaled dot-product attention for self-attention over
+ * [B, H, N, d] tensors ("6.1 FlashAttention V1 in detail", section 1.1 and the
+ * shapes of section 8.1):
+ *
+ *     S = scale * Q K^T          (per batch b and head h, N x N)
+ *     P = softmax(S) row-wise    (causal: key j > query i is excluded)
+ *     O = P V                    ([B, H, N, d])
+ *     LSE_i = m_i + ln(l_i)      (row max m and exp-sum l of S; "FlashAttention:
+ *                                 IO-Aware Tiling, ...", section "Backward Pass
+ *                                 Recomputation", L = m + log(l))
+ *
+ * computed in one fused pass that streams K/V tiles through a running max,
+ * exp-sum and unnormalised output ("FlashAttention: optimize data movement
+ * before counting FLOPs", section 02: m' = max(m, max s),
+ * l' = e^(m-m') l + sum e^(s-m'), u' = e^(m-m') u + sum e^(s-m') V,
+ * Output = u'/l'), so no N x N matrix is ever written to device memory.
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are device pointers on the current CUDA device, owned by the
+ *     caller.  The library allocates no device memory per call.
+ *   - Calls are asynchronous: they enqueue work on `stream` (a cudaStream_t;
+ *     NULL is the legacy default stream) and never synchronise.
+ *   - On any error code the call has launched nothing and written nothing.
+ *   - Thread safety: calls may come from several host threads; the only
+ *     shared state is a per-device status word and cached device properties.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1, /* null/misaligned/overlapping pointer, bad size, bad scale */
+    FA_ERR_UNSUPPORTED = 2, /* a valid problem this build does not handle (d not 64/128) */
+    FA_ERR_NO_DEVICE = 3,   /* no CUDA device, or a pointer not on the current device */
+    FA_ERR_ARCH = 4,        /* the current device is not compute capability 10.3 */
+    FA_ERR_LAUNCH = 5,      /* the kernel launch itself failed (CUDA error) */
+    FA_ERR_TIMEOUT = 6      /* a bounded in-kernel wait gave up (see fa_get_device_status) */
+};
+
+/*
+ * fa_fwd - fused exact attention forward.
+ *
+ *   q, k, v : const bf16, contiguous [B, H, N, d] (row-major, d fastest).
+ *             May alias one another (they are only read).
+ *   o       : bf16 out, contiguous [B, H, N, d]; O = P V rounded once to bf16
+ *             (round-to-nearest-even).
+ *   lse     : fp32 out, contiguous [B, H, N]; natural-log log-sum-exp of the
+ *             scaled logits of each row over its admitted keys.
+ *   B, H, N : batch, heads, sequence length (queries = keys = N); each >= 1,
+ *             B*H*N*d < 2^40.
+ *   d       : head dimension, 64 or 128 (else FA_ERR_UNSUPPORTED).
+ *   scale   : softmax scale, finite and > 0 (1/sqrt(d) in the usual case).
+ *   causal  : 0 = every key admitted; 1 = key j admitted to query i iff j <= i.
+ *   stream  : cudaStream_t to enqueue on.
+ *
+ * Every pointer must be 16-byte aligned and on the current device; o and lse
+ * must not overlap q, k, v or each other.  Work is split into tiles of 128
+ * query rows; ragged N (not a multiple of the tile) is handled in the kernel.
+ * Returns FA_OK or an fa_status code; an error found inside the kernel is
+ * reported later by fa_get_device_status().
+ */
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+           int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
+           void *stream);
+
+/*
+ * fa_get_device_status - synchronise `stream`, then return and clear the
+ * current device's sticky in-kernel status (FA_OK, or FA_ERR_TIMEOUT when a
+ * bounded wait inside a kernel gave up and the kernel returned early, leaving
+ * its outputs incomplete).  Returns FA_ERR_LAUNCH if the synchronisation
+ * itself reports a CUDA error.
+ */
+int fa_get_device_status(void *stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *fa_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */
