@@ -38,8 +38,9 @@ from exact_attention_32_gb300.workloads import HEADLINE, WORKLOADS, workload_inp
 
 METRIC = "attention fwd TFLOPS (bf16, 1×GB300) and % of dense BF16 tensor peak"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
-KERNEL_SOURCES = {"fa_fwd_mma_kernel": "exact_attention_32_gb300/csrc/fa_fwd_mma.cu"}
-DOMINANT_KERNEL = "fa_fwd_mma_kernel"
+KERNEL_SOURCES = {"fa_fwd_tc_kernel": "exact_attention_32_gb300/csrc/fa_fwd_tc.cu",
+                  "fa_fwd_mma_kernel": "exact_attention_32_gb300/csrc/fa_fwd_mma.cu"}
+DOMINANT_KERNEL = "fa_fwd_tc_kernel"
 
 
 def parse_args():

@@ -2,9 +2,9 @@
 
 ``forward(q, k, v, scale=None, causal=False)`` returns (O, LSE) computed by the
 CUDA kernels of ``libfa.so`` (see include/fa.h); the raw C ABI is exposed under
-its own names (``fa_fwd``, ``fa_get_device_status``, ``fa_status_string``,
+its own names (``fa_fwd``, ``fa_fwd_mma``, ``fa_get_device_status``, ``fa_status_string``,
 ``fa_version``).  The library is loaded on first use and its absence raises.
 """
-from ._binding import (FAError, default_scale, fa_fwd, fa_get_device_status,  # noqa: F401
-                       fa_status_string, fa_version, forward, lib)
+from ._binding import (FAError, default_scale, fa_fwd, fa_fwd_mma,  # noqa: F401
+                       fa_get_device_status, fa_status_string, fa_version, forward, lib)
 from .workloads import HEADLINE, WORKLOADS, Workload, make_inputs, workload_inputs  # noqa: F401

@@ -23,7 +23,7 @@ _lock = threading.Lock()
 FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_NO_DEVICE",
                 4: "FA_ERR_ARCH", 5: "FA_ERR_LAUNCH", 6: "FA_ERR_TIMEOUT"}
-EXPORTED = ("fa_fwd", "fa_get_device_status", "fa_status_string", "fa_version")
+EXPORTED = ("fa_fwd", "fa_fwd_mma", "fa_get_device_status", "fa_status_string", "fa_version")
 
 
 class FAError(RuntimeError):
@@ -45,6 +45,8 @@ def lib():
             L.fa_fwd.restype = ctypes.c_int
             L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
                                  ctypes.c_int, vp]
+            L.fa_fwd_mma.restype = ctypes.c_int
+            L.fa_fwd_mma.argtypes = L.fa_fwd.argtypes
             L.fa_get_device_status.restype = ctypes.c_int
             L.fa_get_device_status.argtypes = [vp]
             L.fa_status_string.restype = ctypes.c_char_p
@@ -58,6 +60,11 @@ def lib():
 def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
     """Raw call: pointers as ints, ``stream`` a cudaStream_t as int (0 = legacy default)."""
     return lib().fa_fwd(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), int(causal), stream)
+
+
+def fa_fwd_mma(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
+    """Raw call of the warp-level (mma.sync) kernel; same contract as ``fa_fwd``."""
+    return lib().fa_fwd_mma(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), int(causal), stream)
 
 
 def fa_get_device_status(stream=0) -> int:
@@ -79,13 +86,17 @@ def default_scale(d: int) -> float:
 
 def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
             causal: bool = False, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
-            stream: torch.cuda.Stream | None = None):
+            stream: torch.cuda.Stream | None = None, kernel: str = "tc"):
     """O, LSE = attention(q, k, v) on the GPU through ``fa_fwd``.
 
     q, k, v: bf16 CUDA tensors [B, H, N, d], contiguous.  Returns (O bf16
     [B, H, N, d], LSE fp32 [B, H, N]); ``out``/``lse`` may be given to write
     in place.  Enqueued on ``stream`` (default: torch's current stream).
+    ``kernel="mma"`` runs the warp-level ``fa_fwd_mma`` kernel instead of the
+    tcgen05 ``fa_fwd`` kernel.
     """
+    if kernel not in ("tc", "mma"):
+        raise ValueError("kernel must be 'tc' or 'mma'")
     if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
         raise ValueError("q, k, v must all be [B, H, N, d]")
     for t in (q, k, v):
@@ -104,8 +115,9 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | No
         raise ValueError("lse must be a contiguous fp32 tensor [B, H, N]")
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     with torch.cuda.device(q.device):
-        st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+        call = fa_fwd if kernel == "tc" else fa_fwd_mma
+        st = call(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                     B, H, N, d, float(scale), bool(causal), s.cuda_stream)
     if st != FA_OK:
-        raise FAError(st, "fa_fwd")
+        raise FAError(st, "fa_fwd" if kernel == "tc" else "fa_fwd_mma")
     return out, lse

@@ -66,10 +66,10 @@ bool overlaps(const void *a, uint64_t na, const void *b, uint64_t nb)
     return x < y + nb && y < x + na;
 }
 
-}  // namespace
+typedef cudaError_t (*Launcher)(const FaProblem &, cudaStream_t);
 
-extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
-                      int64_t H, int64_t N, int64_t d, float scale, int causal, void *stream)
+int validate_and_launch(Launcher launch, const void *q, const void *k, const void *v, void *o, float *lse,
+                        int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal, void *stream)
 {
     // sizes first: nothing is touched for an invalid problem
     if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
@@ -106,9 +106,23 @@ extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, floa
     p.scale = scale;
     p.causal = causal;
     p.sm_count = sm_count;
-    const cudaError_t e = fa_launch_mma(p, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = launch(p, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return FA_ERR_LAUNCH;
     return FA_OK;
+}
+
+}  // namespace
+
+extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                      int64_t H, int64_t N, int64_t d, float scale, int causal, void *stream)
+{
+    return validate_and_launch(fa_launch_tc, q, k, v, o, lse, B, H, N, d, scale, causal, stream);
+}
+
+extern "C" int fa_fwd_mma(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                          int64_t H, int64_t N, int64_t d, float scale, int causal, void *stream)
+{
+    return validate_and_launch(fa_launch_mma, q, k, v, o, lse, B, H, N, d, scale, causal, stream);
 }
 
 extern "C" int fa_get_device_status(void *stream)
@@ -117,7 +131,7 @@ extern "C" int fa_get_device_status(void *stream)
         cudaGetLastError();
         return FA_ERR_LAUNCH;
     }
-    return FA_OK;
+    return fa_tc_take_status(static_cast<cudaStream_t>(stream));
 }
 
 extern "C" const char *fa_status_string(int status)

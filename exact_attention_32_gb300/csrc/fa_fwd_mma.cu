@@ -85,6 +85,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
 }
+__device__ __forceinline__ float bf16_lo(uint32_t p) { return __uint_as_float(p << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t p) { return __uint_as_float(p & 0xffff0000u); }
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -132,7 +134,8 @@ fa_fwd_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
     cp_commit();
 
     float m_r[2] = {-INFINITY, -INFINITY};  // running max, unscaled units
-    float l_r[2] = {0.f, 0.f};              // this thread's share of the exp-sum
+    float l_r[2] = {0.f, 0.f};              // this thread's share of the exp-sum (fp32 terms; LSE)
+    float lq_r[2] = {0.f, 0.f};             // the same over the bf16-rounded terms (normalises O)
     float acc[D / 8][4];
 #pragma unroll
     for (int i = 0; i < D / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
@@ -205,6 +208,8 @@ fa_fwd_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
         }
         l_r[0] = l_r[0] * alpha[0] + rs[0];
         l_r[1] = l_r[1] * alpha[1] + rs[1];
+        lq_r[0] *= alpha[0];
+        lq_r[1] *= alpha[1];
 #pragma unroll
         for (int i = 0; i < D / 8; ++i) {
             acc[i][0] *= alpha[0];
@@ -221,6 +226,8 @@ fa_fwd_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
             const uint32_t a1 = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
             const uint32_t a2 = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
             const uint32_t a3 = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+            lq_r[0] += bf16_lo(a0) + bf16_hi(a0) + bf16_lo(a2) + bf16_hi(a2);
+            lq_r[1] += bf16_lo(a1) + bf16_hi(a1) + bf16_lo(a3) + bf16_hi(a3);
 #pragma unroll
             for (int nd = 0; nd < D / 16; ++nd) {
                 uint32_t b0, b1, b2, b3;
@@ -232,15 +239,18 @@ fa_fwd_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
         __syncthreads();  // this stage is refilled two iterations later
     }
 
-    // epilogue: O = u / l (bf16), LSE = m * scale + ln(l)
+    // epilogue: O = u / l (bf16), LSE = m * scale + ln(l).  u was accumulated
+    // from bf16-rounded P, so it is divided by the sum of those rounded terms.
     float inv[2], lrow[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-        float l = l_r[r];
+        float l = l_r[r], lq = lq_r[r];
         l += __shfl_xor_sync(0xffffffffu, l, 1);
         l += __shfl_xor_sync(0xffffffffu, l, 2);
+        lq += __shfl_xor_sync(0xffffffffu, lq, 1);
+        lq += __shfl_xor_sync(0xffffffffu, lq, 2);
         lrow[r] = l;
-        inv[r] = 1.f / l;
+        inv[r] = 1.f / lq;
     }
     const int gr0 = q0 + row_w + g, gr1 = gr0 + 8;
     __nv_bfloat16 *oh = o + base;

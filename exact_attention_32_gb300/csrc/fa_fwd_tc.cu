@@ -1,0 +1,447 @@
+// Fused exact attention forward for GB300 (sm_103a): TMA + tcgen05 + TMEM.
+//
+// What is computed (per batch b, head h, query row i):
+//   S_ij = scale * q_i . k_j,  P_i = softmax(S_i) over admitted keys,
+//   O_i = sum_j P_ij v_j,      LSE_i = m_i + ln(l_i)
+// ("6.1 FlashAttention V1 in detail", sections 1.1 and 5.1; LSE as in
+// "FlashAttention: IO-Aware Tiling, ...", section "Backward Pass Recomputation").
+//
+// How: each CTA owns 2 query tiles of 128 rows (256 consecutive rows of one
+// (b, h) slice) and streams the admitted 128-key K/V tiles once for both.
+// Per K/V tile j and query tile t the running statistics are merged as in
+// "FlashAttention: optimize data movement before counting FLOPs", section 02
+// (m' = max(m, max s), l' = e^(m-m') l + sum e^(s-m'), u' = e^(m-m') u + P V):
+// the numerator u lives in tensor memory and is divided by l once at the end
+// (the FlashAttention-2 rescaling optimisation on the llms.blog page).
+//
+// Roles (320 threads):
+//   warps 0-3  softmax warpgroup of query tile 0 (one thread per row)
+//   warps 4-7  softmax warpgroup of query tile 1
+//   warp  8    TMA producer: Q tiles once, then K_j, V_j into a ring of slots
+//   warp  9    tcgen05 issuer (and TMEM owner):
+//                S_t  = Q_t K_j^T          (A, B from shared memory)
+//                O_t += P_t V_j            (A = P from tensor memory)
+// Tensor memory (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256),
+// O_0 [256,256+d), O_1 [384,384+d); P_t (bf16, two per column) overwrites the
+// first 64 columns of S_t once S_t has been read.
+//
+// Exponentials are base 2 with scale*log2(e) folded into one FMA; the
+// reference max m is kept in unscaled dot-product units (scale > 0).  The
+// numerator is rescaled only when the row max grows by more than 2^8 (any
+// common shift of a row's logits leaves softmax unchanged - the identity of
+// "6.1 ...", section 3.3 - so a stale reference is exact as long as the
+// exponentials stay in range; LSE = m_ref + ln(l) holds for any reference).
+// Keys >= N and, when causal, keys j > i are set to -inf before the max
+// ("6.1 ...", section 8.3: the K/V out-of-range mask).
+//
+// Every mbarrier wait is bounded; a wait that gives up sets FA_ERR_TIMEOUT in
+// a device status word and the CTA winds down (waiting, bounded, for its own
+// copies and MMAs in flight, then freeing its tensor memory).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "fa.h"
+#include "fa_internal.h"
+#include "sm100_ptx.cuh"
+
+using namespace sm100;
+
+namespace {
+
+constexpr int kBlockM = 128;  // query rows per query tile
+constexpr int kBlockN = 128;  // keys per K/V tile
+constexpr int kQTiles = 2;    // query tiles per CTA
+constexpr int kThreads = 320;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kRescaleLog2 = 8.0f;            // rescale when the max grows by more than 2^8
+constexpr uint64_t kWaitLimitNs = 1000000000ull;    // 1 s per pipeline wait
+constexpr uint64_t kCleanupLimitNs = 20000000ull;    // 20 ms per wait while winding down
+
+__device__ int g_tc_status;  // sticky FA_ERR_TIMEOUT, read and cleared by fa_get_device_status
+
+template <int D>
+struct Cfg {
+    static constexpr int kTileBytes = kBlockN * D * 2;  // one Q, K or V tile (bf16)
+    static constexpr int kAtoms = D / 64;               // 128-byte-wide column blocks per tile
+    static constexpr int kStages = D == 128 ? 4 : 8;    // K/V ring slots
+    static constexpr int kBarOffset = (kQTiles + kStages) * kTileBytes;
+    // barriers: q_full, s_full[2], p_full[2], o_full[2], mma_done, kv_full[S], kv_empty[S]
+    static constexpr int kNumBars = 8 + 2 * kStages;
+    static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
+};
+
+struct Bars {
+    uint32_t q_full, s_full[2], p_full[2], o_full[2], mma_done, kv_full, kv_empty;
+    __device__ uint32_t full(int s) const { return kv_full + 8u * s; }
+    __device__ uint32_t empty(int s) const { return kv_empty + 8u * s; }
+};
+
+__device__ __forceinline__ void report_timeout() { atomicExch(&g_tc_status, FA_ERR_TIMEOUT); }
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                 float *__restrict__ lse, int N, int BH, int n_mblocks, float scale, float scale_log2)
+{
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s_base = smem_u32(smem);
+    const uint32_t sQ = s_base;                         // kQTiles tiles
+    const uint32_t sRing = s_base + kQTiles * C::kTileBytes;
+    const uint32_t bar0 = s_base + C::kBarOffset;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kBarOffset + C::kNumBars * 8);
+
+    Bars bars;
+    bars.q_full = bar0;
+    bars.s_full[0] = bar0 + 8;
+    bars.s_full[1] = bar0 + 16;
+    bars.p_full[0] = bar0 + 24;
+    bars.p_full[1] = bar0 + 32;
+    bars.o_full[0] = bar0 + 40;
+    bars.o_full[1] = bar0 + 48;
+    bars.mma_done = bar0 + 56;
+    bars.kv_full = bar0 + 64;
+    bars.kv_empty = bar0 + 64 + 8 * C::kStages;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // work unit: 256 query rows of one (b, h); causal: heaviest row blocks first
+    const int unit = blockIdx.x;
+    const int mb = CAUSAL ? (n_mblocks - 1 - unit / BH) : (unit / BH);
+    const int bh = unit % BH;
+    const int q_row0 = mb * (kQTiles * kBlockM);
+    const int kv_end = CAUSAL ? min(N, q_row0 + kQTiles * kBlockM) : N;
+    const int n_kv = (kv_end + kBlockN - 1) / kBlockN;
+    // after a timeout anywhere (sticky until read by the host) CTAs do no work
+    const bool run = n_kv > 0 && *reinterpret_cast<volatile int *>(&g_tc_status) == 0;
+
+    if (tid == 0) {
+        mbar_init(bars.q_full, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bars.s_full[t], 1);
+            mbar_init(bars.p_full[t], kBlockM);
+            mbar_init(bars.o_full[t], 1);
+        }
+        mbar_init(bars.mma_done, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bars.full(s), 1);
+            mbar_init(bars.empty(s), 1);
+        }
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (!run) {
+        // nothing to do: fall through to the teardown
+    } else if (warp == kLoadWarp) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_arrive_expect_tx(bars.q_full, kQTiles * C::kTileBytes);
+            for (int t = 0; t < kQTiles; ++t)
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &tm_q, bars.q_full, a * 64,
+                                q_row0 + t * kBlockM, bh);
+            bool ok = true;
+            int it = 0;
+            for (int j = 0; j < n_kv && ok; ++j) {
+                for (int kind = 0; kind < 2 && ok; ++kind, ++it) {
+                    const int slot = it % C::kStages, use = it / C::kStages;
+                    if (!mbar_wait(bars.empty(slot), (use & 1) ^ 1, kWaitLimitNs)) {
+                        ok = false;
+                        report_timeout();
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
+                    const CUtensorMap *tm = kind == 0 ? &tm_k : &tm_v;
+                    for (int a = 0; a < C::kAtoms; ++a)
+                        tma_load_3d(sRing + slot * C::kTileBytes + a * 16384, tm, bars.full(slot), a * 64,
+                                    j * kBlockN, bh);
+                }
+            }
+            // every copy this thread issued has landed before the CTA may exit
+            const uint64_t lim = ok ? kWaitLimitNs : kCleanupLimitNs;
+            mbar_wait(bars.q_full, 0, lim);
+            for (int k = max(0, it - C::kStages); k < it; ++k)
+                mbar_wait(bars.full(k % C::kStages), (k / C::kStages) & 1, lim);
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(kBlockM, kBlockN, false);
+            constexpr uint32_t idO = idesc_bf16_f32(kBlockM, D, true);
+            bool ok = mbar_wait(bars.q_full, 0, kWaitLimitNs);
+            tc_fence_after();
+            int it = 0, prev_v = -1;
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int kslot = it % C::kStages, kuse = it / C::kStages;
+                ++it;
+                const int vslot = it % C::kStages, vuse = it / C::kStages;
+                ++it;
+                if (!(ok = mbar_wait(bars.full(kslot), kuse & 1, kWaitLimitNs))) break;
+                tc_fence_after();
+                const uint32_t kaddr = sRing + kslot * C::kTileBytes;
+                for (int t = 0; t < kQTiles && ok; ++t) {
+                    if (j > 0) {
+                        if (!(ok = mbar_wait(bars.p_full[t], (j - 1) & 1, kWaitLimitNs))) break;
+                        tc_fence_after();
+                        const uint32_t vaddr = sRing + prev_v * C::kTileBytes;
+#pragma unroll
+                        for (int kk = 0; kk < kBlockN / 16; ++kk)
+                            mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
+                                   smem_desc_sw128(vaddr + kk * 16 * 128, kBlockN * 128, 1024), idO,
+                                   (j > 1 || kk > 0) ? 1u : 0u);
+                    }
+                    const uint32_t qaddr = sQ + t * C::kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t koff = (kk / 4) * 16384 + (kk % 4) * 32;
+                        mma_ss(tmem + t * 128, smem_desc_sw128(qaddr + koff, 16, 1024),
+                               smem_desc_sw128(kaddr + koff, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bars.s_full[t]);
+                }
+                if (!ok) break;
+                mma_commit(bars.empty(kslot));
+                if (j > 0) mma_commit(bars.empty(prev_v));
+                if (!(ok = mbar_wait(bars.full(vslot), vuse & 1, kWaitLimitNs))) break;
+                tc_fence_after();
+                prev_v = vslot;
+            }
+            for (int t = 0; t < kQTiles && ok; ++t) {
+                if (!(ok = mbar_wait(bars.p_full[t], (n_kv - 1) & 1, kWaitLimitNs))) break;
+                tc_fence_after();
+                const uint32_t vaddr = sRing + prev_v * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk)
+                    mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
+                           smem_desc_sw128(vaddr + kk * 16 * 128, kBlockN * 128, 1024), idO,
+                           (n_kv > 1 || kk > 0) ? 1u : 0u);
+                mma_commit(bars.o_full[t]);
+            }
+            if (ok) mma_commit(bars.empty(prev_v));
+            if (!ok) report_timeout();
+            // no MMA of this CTA may still be running when tensor memory is freed
+            mma_commit(bars.mma_done);
+            mbar_wait(bars.mma_done, 0, ok ? kWaitLimitNs : kCleanupLimitNs);
+        }
+    } else {
+        // --------------------------------------------------------------- softmax
+        const int t = warp >> 2;          // query tile of this warpgroup
+        const int row = tid & 127;        // row within the tile == TMEM lane
+        const int row_g = q_row0 + t * kBlockM + row;
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_off + t * 128;
+        const uint32_t tO = tmem + lane_off + 256 + t * 128;
+        float m_ref = -INFINITY;  // reference max, unscaled units
+        float l = 0.f;            // exp-sum relative to m_ref (fp32 terms; gives LSE)
+        float lr = 0.f;           // the same sum over the bf16-rounded terms the MMA sees (normalises O)
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            if (!mbar_wait(bars.s_full[t], j & 1, kWaitLimitNs)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float s[kBlockN];
+            {
+                uint32_t r[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, r[c]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
+            }
+            const int k0 = j * kBlockN;
+            const bool need_mask = (k0 + kBlockN > N) || (CAUSAL && k0 + kBlockN - 1 > q_row0 + t * kBlockM);
+            if (need_mask) {
+                const int lim = CAUSAL ? min(N - 1, row_g) : N - 1;  // last admitted key
+#pragma unroll
+                for (int i = 0; i < kBlockN; ++i)
+                    if (k0 + i > lim) s[i] = -INFINITY;
+            }
+            float mt = s[0];
+#pragma unroll
+            for (int i = 1; i < kBlockN; ++i) mt = fmaxf(mt, s[i]);
+            const float m_new = fmaxf(m_ref, mt);
+            const bool need = (m_new - m_ref) * scale_log2 > kRescaleLog2;  // true while m_ref = -inf
+            float alpha = 1.f;
+            if (need) {
+                alpha = ex2((m_ref - m_new) * scale_log2);  // 0 on the first tile
+                m_ref = m_new;
+                l *= alpha;
+                lr *= alpha;
+            }
+            // P = exp2(s * scale * log2 e - m_ref * scale * log2 e), bf16, over the first 64 columns of S_t
+            const float mc = (m_ref == -INFINITY ? 0.f : m_ref) * scale_log2;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t p[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = ex2(fmaf(s[c * 32 + 2 * i], scale_log2, -mc));
+                    const float p1 = ex2(fmaf(s[c * 32 + 2 * i + 1], scale_log2, -mc));
+                    l += p0 + p1;
+                    p[i] = pack_bf16x2(p0, p1);
+                    lr += __uint_as_float(p[i] << 16) + __uint_as_float(p[i] & 0xffff0000u);
+                }
+                tmem_st16(tS + c * 16, p);
+            }
+            // numerator rescale u *= alpha (u holds P V up to tile j-1, complete: the
+            // commit that signalled S_t(j) was issued after that MMA); nothing to scale at j = 0
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tO + c * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                    tmem_st32(tO + c * 32, r);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bars.p_full[t]);
+        }
+        if (ok) ok = mbar_wait(bars.o_full[t], 0, kWaitLimitNs);
+        if (!ok) report_timeout();
+        tc_fence_after();
+        // epilogue: O = u / l in bf16, staged (128-byte swizzle) in this tile's Q buffer.
+        // u was accumulated from bf16-rounded P, so it is divided by the sum of
+        // those same rounded terms: the weights then sum to one exactly and a
+        // row dominated by one key returns that key's value without a P-rounding error.
+        const float inv_l = 1.f / lr;
+        uint8_t *stage = smem + t * C::kTileBytes;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tO + c * 32, r);
+            tmem_wait_ld();
+            const int a = c / 2;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const int chunk = (c % 2) * 4 + q4;
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(r[q4 * 8 + 0]) * inv_l, __uint_as_float(r[q4 * 8 + 1]) * inv_l);
+                v.y = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2]) * inv_l, __uint_as_float(r[q4 * 8 + 3]) * inv_l);
+                v.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * inv_l, __uint_as_float(r[q4 * 8 + 5]) * inv_l);
+                v.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * inv_l, __uint_as_float(r[q4 * 8 + 7]) * inv_l);
+                *reinterpret_cast<uint4 *>(stage + a * 16384 + row * 128 + ((chunk ^ (row & 7)) * 16)) = v;
+            }
+        }
+        if (row_g < N && ok) lse[static_cast<int64_t>(bh) * N + row_g] = m_ref * scale + logf(l);
+        fence_proxy_async_smem();
+        named_bar_sync(1 + t, kBlockM);
+        if (row == 0 && ok && q_row0 + t * kBlockM < N) {
+            for (int a = 0; a < C::kAtoms; ++a)
+                tma_store_3d(&tm_o, smem_u32(stage) + a * 16384, a * 64, q_row0 + t * kBlockM, bh);
+            bulk_commit();
+            bulk_wait0();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// [BH][N][d] bf16 viewed as a 3-D tensor (d fastest); box = 64 columns x 128 rows x 1 slice.
+bool make_map(CUtensorMap *m, const void *base, int64_t BH, int64_t N, int d)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch(const FaProblem &p, cudaStream_t stream)
+{
+    using C = Cfg<D>;
+    CUtensorMap mq, mk, mv, mo;
+    const int64_t BH = p.B * p.H;
+    if (!make_map(&mq, p.q, BH, p.N, D) || !make_map(&mk, p.k, BH, p.N, D) || !make_map(&mv, p.v, BH, p.N, D) ||
+        !make_map(&mo, p.o, BH, p.N, D))
+        return cudaErrorInvalidValue;
+    auto kern = fa_fwd_tc_kernel<D, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int64_t n_mblocks = (p.N + kQTiles * kBlockM - 1) / (kQTiles * kBlockM);
+    const int64_t blocks = n_mblocks * BH;
+    if (blocks > 0x7fffffffLL || BH > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
+    kern<<<static_cast<unsigned>(blocks), kThreads, C::kSmemBytes, stream>>>(
+        mq, mk, mv, mo, p.lse, static_cast<int>(p.N), static_cast<int>(BH), static_cast<int>(n_mblocks), p.scale,
+        scale_log2);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t fa_launch_tc(const FaProblem &p, cudaStream_t stream)
+{
+    if (p.d == 64) return p.causal ? launch<64, true>(p, stream) : launch<64, false>(p, stream);
+    return p.causal ? launch<128, true>(p, stream) : launch<128, false>(p, stream);
+}
+
+int fa_tc_take_status(cudaStream_t stream)
+{
+    int h = 0;
+    const int zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&h, g_tc_status, sizeof(int), 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_tc_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_LAUNCH;
+    }
+    return h;
+}

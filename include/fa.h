@@ -74,11 +74,23 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            void *stream);
 
 /*
+ * fa_fwd_mma - the same operation, arguments, layouts and errors as fa_fwd,
+ * computed by a warp-level tensor-core kernel (mma.sync m16n8k16, one CTA per
+ * 128 query rows, cp.async double buffering) instead of the tcgen05 kernel.
+ * Kept as an independent second implementation for cross-checks and as the
+ * performance baseline of the pre-tcgen05 tensor-core path.
+ */
+int fa_fwd_mma(const void *q, const void *k, const void *v, void *o, float *lse,
+               int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
+               void *stream);
+
+/*
  * fa_get_device_status - synchronise `stream`, then return and clear the
  * current device's sticky in-kernel status (FA_OK, or FA_ERR_TIMEOUT when a
  * bounded wait inside a kernel gave up and the kernel returned early, leaving
- * its outputs incomplete).  Returns FA_ERR_LAUNCH if the synchronisation
- * itself reports a CUDA error.
+ * its outputs incomplete).  While FA_ERR_TIMEOUT is set, fa_fwd launches do
+ * no work (their outputs are left unwritten) until this call clears it.
+ * Returns FA_ERR_LAUNCH if the synchronisation itself reports a CUDA error.
  */
 int fa_get_device_status(void *stream);
 

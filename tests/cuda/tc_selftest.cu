@@ -1,0 +1,142 @@
+// Test-only check of the tcgen05 operand layouts the attention kernel relies on.
+//
+// One CTA of 128 threads:
+//   1. Q, K, V (128 x D bf16, row-major in global memory) are written into
+//      shared memory in the 128-byte-swizzled layout a TMA tile load with
+//      128-byte swizzle produces: D/64 column blocks of [128 rows][128 bytes],
+//      16-byte chunk c of row r stored at chunk position c ^ (r % 8).
+//   2. S = Q K^T: tcgen05.mma (A and B from shared memory, both K-major),
+//      accumulated in TMEM columns [0, 128); every thread reads its row back.
+//   3. P = bf16(S) is written over TMEM columns [0, 64) (two bf16 per column)
+//      and O = P V is computed with A from TMEM and V as an MN-major B operand.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "sm100_ptx.cuh"
+
+using namespace sm100;
+
+template <int D>
+__global__ void __launch_bounds__(128, 1)
+tc_selftest_kernel(const uint16_t *q, const uint16_t *k, const uint16_t *v, float *s_out, float *o_out,
+                   int *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr int TILE = 128 * D * 2;
+    uint8_t *sQ = smem, *sK = smem + TILE, *sV = smem + 2 * TILE;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + 3 * TILE);
+    uint32_t *tmem_base_slot = reinterpret_cast<uint32_t *>(smem + 3 * TILE + 16);
+    const int tid = threadIdx.x, warp = tid / 32;
+
+    // 1. swizzled tiles
+    for (int idx = tid; idx < 128 * (D / 8); idx += 128) {
+        const int r = idx / (D / 8), c = idx % (D / 8);  // 16-byte chunk c of row r
+        const int blk = c / 8, cc = c % 8;
+        const uint32_t off = blk * (128 * 128) + r * 128 + ((cc ^ (r % 8)) * 16);
+        const uint4 *src_q = reinterpret_cast<const uint4 *>(q + r * D + c * 8);
+        const uint4 *src_k = reinterpret_cast<const uint4 *>(k + r * D + c * 8);
+        const uint4 *src_v = reinterpret_cast<const uint4 *>(v + r * D + c * 8);
+        *reinterpret_cast<uint4 *>(sQ + off) = *src_q;
+        *reinterpret_cast<uint4 *>(sK + off) = *src_k;
+        *reinterpret_cast<uint4 *>(sV + off) = *src_v;
+    }
+    fence_proxy_async_smem();
+    if (tid == 0) {
+        mbar_init(smem_u32(bar), 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_base_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_base_slot;
+    const uint32_t tS = tbase, tO = tbase + 256;
+
+    // 2. S = Q K^T
+    if (tid == 0) {
+        constexpr uint32_t idS = idesc_bf16_f32(128, 128, false);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk / 4) * (128 * 128) + (kk % 4) * 32;
+            mma_ss(tS, smem_desc_sw128(smem_u32(sQ) + koff, 16, 1024),
+                   smem_desc_sw128(smem_u32(sK) + koff, 16, 1024), idS, kk > 0);
+        }
+        mma_commit(smem_u32(bar));
+    }
+    __syncwarp();
+    bool ok = mbar_wait(smem_u32(bar), 0, 2000000000ull);
+    tc_fence_after();
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int row = tid;
+    float srow[128];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tS + lane_off + c * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) srow[c * 32 + i] = __uint_as_float(r[i]);
+    }
+    for (int i = 0; i < 128; ++i) s_out[row * 128 + i] = srow[i];
+
+    // 3. P = bf16(S) into TMEM columns [0, 64), then O = P V
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t p[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(srow[c * 32 + 2 * i], srow[c * 32 + 2 * i + 1]);
+        tmem_st16(tS + lane_off + c * 16, p);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        constexpr uint32_t idO = idesc_bf16_f32(128, D, true);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tO, tS + kk * 8, smem_desc_sw128(smem_u32(sV) + kk * 16 * 128, 128 * 128, 1024), idO, kk > 0);
+        mma_commit(smem_u32(bar));
+    }
+    __syncwarp();
+    ok = mbar_wait(smem_u32(bar), 1, 2000000000ull) && ok;
+    tc_fence_after();
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tO + lane_off + c * 32, r);
+        tmem_wait_ld();
+        for (int i = 0; i < 32; ++i) o_out[row * D + c * 32 + i] = __uint_as_float(r[i]);
+    }
+    if (!ok) atomicExch(status, 6);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
+extern "C" int tc_selftest(const void *q, const void *k, const void *v, float *s_out, float *o_out, int *status,
+                           int d)
+{
+    const int smem = 3 * 128 * d * 2 + 1024 + 64;
+    cudaError_t e;
+    if (d == 64) {
+        e = cudaFuncSetAttribute(tc_selftest_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            tc_selftest_kernel<64><<<1, 128, smem>>>(static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k),
+                                                     static_cast<const uint16_t *>(v), s_out, o_out, status);
+    } else if (d == 128) {
+        e = cudaFuncSetAttribute(tc_selftest_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            tc_selftest_kernel<128><<<1, 128, smem>>>(static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k),
+                                                      static_cast<const uint16_t *>(v), s_out, o_out, status);
+    } else {
+        return -1;
+    }
+    if (e != cudaSuccess) return static_cast<int>(e);
+    e = cudaDeviceSynchronize();
+    return static_cast<int>(e);
+}

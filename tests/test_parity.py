@@ -7,12 +7,16 @@ Tolerances (bf16 inputs and output, fp32 accumulation):
 Small problems are compared on every row; the full-size workloads on sampled
 rows (first/last rows, both sides of every 128-row tile boundary, random rows).
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from exact_attention_32_gb300 import WORKLOADS, forward, make_inputs, workload_inputs
+from exact_attention_32_gb300 import (WORKLOADS, fa_get_device_status, forward, make_inputs,
+                                      workload_inputs)
 from exact_attention_32_gb300.workloads import sample_rows
 
 MAX_O, MEAN_O, MAX_LSE = 2e-2, 2e-3, 1e-3
@@ -20,12 +24,16 @@ MAX_O, MEAN_O, MAX_LSE = 2e-2, 2e-3, 1e-3
 pytestmark = pytest.mark.gpu
 
 
-def run_gpu(q, k, v, scale, causal):
+KERNELS = ["tc", "mma"]
+
+
+def run_gpu(q, k, v, scale, causal, kernel="tc"):
     qd, kd, vd = (t.cuda() for t in (q, k, v))
     o = torch.full_like(qd, float("nan"))
     lse = torch.full(qd.shape[:3], float("nan"), dtype=torch.float32, device="cuda")
-    forward(qd, kd, vd, scale=scale, causal=causal, out=o, lse=lse)
+    forward(qd, kd, vd, scale=scale, causal=causal, out=o, lse=lse, kernel=kernel)
     torch.cuda.synchronize()
+    assert fa_get_device_status(0) == 0
     return o.double().cpu().numpy(), lse.double().cpu().numpy()
 
 
@@ -33,38 +41,47 @@ def check(o_gpu, lse_gpu, o_ref, lse_ref):
     assert np.isfinite(o_gpu).all() and np.isfinite(lse_gpu).all(), "unwritten or non-finite output"
     err = np.abs(o_gpu - o_ref)
     lerr = np.abs(lse_gpu - lse_ref)
+    log = os.environ.get("FA_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"test": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0],
+                                "max_dO": float(err.max()), "mean_dO": float(err.mean()),
+                                "max_dLSE": float(lerr.max())}) + "\n")
     assert err.max() <= MAX_O, f"max|dO| = {err.max():.3e}"
     assert err.mean() <= MEAN_O, f"mean|dO| = {err.mean():.3e}"
     assert lerr.max() <= MAX_LSE, f"max|dLSE| = {lerr.max():.3e}"
     return err.max(), err.mean(), lerr.max()
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("N", [1, 2, 63, 127, 128, 129, 255, 257, 1000])
-def test_small_problems_every_row(N, d, causal):
+@pytest.mark.parametrize("N", [1, 2, 63, 127, 128, 129, 255, 256, 257, 383, 384, 385, 1000])
+def test_small_problems_every_row(N, d, causal, kernel):
     q, k, v = make_inputs(2, 3, N, d, seed=N * 7 + d + causal)
     scale = float(np.float32(1 / np.sqrt(d)))
-    o, lse = run_gpu(q, k, v, scale, causal)
+    o, lse = run_gpu(q, k, v, scale, causal, kernel)
     o_ref, lse_ref = oracle.attention(q, k, v, scale, causal)
     check(o, lse, o_ref, lse_ref)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("name", ["b1_h1_n256_d64", "b16_h16_n1000_d64_causal_q8"])
-def test_workload_every_row(name):
+def test_workload_every_row(name, kernel):
     w = WORKLOADS[name]
     q, k, v = workload_inputs(w)
-    o, lse = run_gpu(q, k, v, w.scale, w.causal)
+    o, lse = run_gpu(q, k, v, w.scale, w.causal, kernel)
     o_ref, lse_ref = oracle.attention(q, k, v, w.scale, w.causal)
     check(o, lse, o_ref, lse_ref)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("name", ["b4_h16_n2048_d128", "b2_h32_n4096_d128_causal",
                                   "b1_h32_n16384_d128_causal", "b1_h32_n16384_d128"])
-def test_workload_sampled_rows(name):
+def test_workload_sampled_rows(name, kernel):
     w = WORKLOADS[name]
     q, k, v = workload_inputs(w)
-    o, lse = run_gpu(q, k, v, w.scale, w.causal)
+    o, lse = run_gpu(q, k, v, w.scale, w.causal, kernel)
     per_head = 24 if w.N >= 16384 else 40
     rows = sample_rows(w.B, w.H, w.N, per_head=per_head, seed=w.seed)
     o_ref, lse_ref = oracle.attention(q, k, v, w.scale, w.causal, rows=rows)
@@ -75,11 +92,12 @@ def test_workload_sampled_rows(name):
     assert np.abs(o).max() <= vmax * (1 + 2 ** -7)
 
 
-def test_large_logit_rows_are_sharp():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_large_logit_rows_are_sharp(kernel):
     # Q x 8: logits reach about +-50; the result still matches where P is
     # nearly one-hot
     q, k, v = make_inputs(1, 4, 700, 64, seed=77, q_gain=8.0)
-    o, lse = run_gpu(q, k, v, 0.125, True)
+    o, lse = run_gpu(q, k, v, 0.125, True, kernel)
     o_ref, lse_ref = oracle.attention(q, k, v, 0.125, True)
     check(o, lse, o_ref, lse_ref)
     assert np.abs(lse_ref).max() > 20
@@ -94,10 +112,11 @@ def test_inputs_may_alias():
     check(o.double().cpu().numpy(), lse.double().cpu().numpy(), o_ref, lse_ref)
 
 
-def test_deterministic():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_deterministic(kernel):
     q, k, v = (t.cuda() for t in make_inputs(2, 4, 1000, 128, seed=6))
-    o1, l1 = forward(q, k, v, causal=True)
-    o2, l2 = forward(q, k, v, causal=True)
+    o1, l1 = forward(q, k, v, causal=True, kernel=kernel)
+    o2, l2 = forward(q, k, v, causal=True, kernel=kernel)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 

@@ -1,0 +1,52 @@
+"""tcgen05 operand layouts the attention kernel relies on, checked bit-exactly
+on small-integer data (every product and sum is exact in fp32):
+S = Q K^T with both operands K-major and 128-byte swizzled in shared memory,
+then P = bf16(S) written into tensor memory over S, and O = P V with P read
+from tensor memory and V an MN-major shared-memory operand."""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_32_gb300 import build as fa_build
+
+pytestmark = pytest.mark.gpu
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module")
+def selftest_lib():
+    out_dir = os.path.join(HERE, "_build")
+    os.makedirs(out_dir, exist_ok=True)
+    so = os.path.join(out_dir, "libtcselftest.so")
+    subprocess.run([fa_build.nvcc()] + fa_build.ARCH +
+                   ["-O2", "-std=c++17", "-Xcompiler", "-fPIC", "-shared", "-I", fa_build.CSRC,
+                    os.path.join(HERE, "cuda", "tc_selftest.cu"), "-o", so], check=True)
+    lib = ctypes.CDLL(so)
+    lib.tc_selftest.restype = ctypes.c_int
+    lib.tc_selftest.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_int]
+    return lib
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_mma_layouts_bit_exact(selftest_lib, d):
+    g = torch.Generator().manual_seed(d)
+    q = torch.randint(-2, 3, (128, d), generator=g).to(torch.bfloat16)
+    k = torch.randint(-2, 3, (128, d), generator=g).to(torch.bfloat16)
+    v = torch.randint(-2, 3, (128, d), generator=g).to(torch.bfloat16)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    s_out = torch.full((128, 128), float("nan"), device="cuda")
+    o_out = torch.full((128, d), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = selftest_lib.tc_selftest(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), s_out.data_ptr(),
+                                  o_out.data_ptr(), status.data_ptr(), d)
+    assert rc == 0
+    assert int(status.item()) == 0
+    s_ref = q.double() @ k.double().T
+    assert torch.equal(s_out.cpu().double(), s_ref), "S = Q K^T layout mismatch"
+    p = s_ref.float().to(torch.bfloat16).double()
+    o_ref = p @ v.double()
+    assert torch.equal(o_out.cpu().double(), o_ref), "O = P V layout mismatch"
