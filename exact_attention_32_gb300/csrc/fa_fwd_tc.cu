@@ -75,10 +75,18 @@ struct Cfg {
     static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
 };
 
+// Shared-memory addresses of the mbarriers, laid out from `base`:
+// q_full, s_full[2], p_full[2], o_full[2], mma_done, kv_full[S], kv_empty[S].
+template <int STAGES>
 struct Bars {
-    uint32_t q_full, s_full[2], p_full[2], o_full[2], mma_done, kv_full, kv_empty;
-    __device__ uint32_t full(int s) const { return kv_full + 8u * s; }
-    __device__ uint32_t empty(int s) const { return kv_empty + 8u * s; }
+    uint32_t base;
+    __device__ uint32_t q_full() const { return base; }
+    __device__ uint32_t s_full(int t) const { return base + 8u + 8u * t; }
+    __device__ uint32_t p_full(int t) const { return base + 24u + 8u * t; }
+    __device__ uint32_t o_full(int t) const { return base + 40u + 8u * t; }
+    __device__ uint32_t mma_done() const { return base + 56u; }
+    __device__ uint32_t full(int s) const { return base + 64u + 8u * s; }
+    __device__ uint32_t empty(int s) const { return base + 64u + 8u * (STAGES + s); }
 };
 
 __device__ __forceinline__ void report_timeout() { atomicExch(&g_tc_status, FA_ERR_TIMEOUT); }
@@ -98,17 +106,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const uint32_t bar0 = s_base + C::kBarOffset;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kBarOffset + C::kNumBars * 8);
 
-    Bars bars;
-    bars.q_full = bar0;
-    bars.s_full[0] = bar0 + 8;
-    bars.s_full[1] = bar0 + 16;
-    bars.p_full[0] = bar0 + 24;
-    bars.p_full[1] = bar0 + 32;
-    bars.o_full[0] = bar0 + 40;
-    bars.o_full[1] = bar0 + 48;
-    bars.mma_done = bar0 + 56;
-    bars.kv_full = bar0 + 64;
-    bars.kv_empty = bar0 + 64 + 8 * C::kStages;
+    const Bars<C::kStages> bars{bar0};
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -123,13 +121,13 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const bool run = n_kv > 0 && *reinterpret_cast<volatile int *>(&g_tc_status) == 0;
 
     if (tid == 0) {
-        mbar_init(bars.q_full, 1);
+        mbar_init(bars.q_full(), 1);
         for (int t = 0; t < 2; ++t) {
-            mbar_init(bars.s_full[t], 1);
-            mbar_init(bars.p_full[t], kBlockM);
-            mbar_init(bars.o_full[t], 1);
+            mbar_init(bars.s_full(t), 1);
+            mbar_init(bars.p_full(t), kBlockM / 32);  // one arrive per softmax warp
+            mbar_init(bars.o_full(t), 1);
         }
-        mbar_init(bars.mma_done, 1);
+        mbar_init(bars.mma_done(), 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bars.full(s), 1);
             mbar_init(bars.empty(s), 1);
@@ -153,10 +151,10 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            mbar_arrive_expect_tx(bars.q_full, kQTiles * C::kTileBytes);
+            mbar_arrive_expect_tx(bars.q_full(), kQTiles * C::kTileBytes);
             for (int t = 0; t < kQTiles; ++t)
                 for (int a = 0; a < C::kAtoms; ++a)
-                    tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &tm_q, bars.q_full, a * 64,
+                    tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &tm_q, bars.q_full(), a * 64,
                                 q_row0 + t * kBlockM, bh);
             bool ok = true;
             int it = 0;
@@ -177,7 +175,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             // every copy this thread issued has landed before the CTA may exit
             const uint64_t lim = ok ? kWaitLimitNs : kCleanupLimitNs;
-            mbar_wait(bars.q_full, 0, lim);
+            mbar_wait(bars.q_full(), 0, lim);
             for (int k = max(0, it - C::kStages); k < it; ++k)
                 mbar_wait(bars.full(k % C::kStages), (k / C::kStages) & 1, lim);
         }
@@ -186,9 +184,20 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(kBlockM, kBlockN, false);
             constexpr uint32_t idO = idesc_bf16_f32(kBlockM, D, true);
-            bool ok = mbar_wait(bars.q_full, 0, kWaitLimitNs);
+            // descriptors are built once; a K step only moves the start address
+            // (low 32 bits, in 16-byte units): +32 bytes inside a 128-byte-wide
+            // column block, +16 KB to the next block (S), +2 KB per 16 keys (P V)
+            const uint64_t dq = smem_desc_sw128(sQ, 16, 1024);
+            const uint64_t dk0 = smem_desc_sw128(sRing, 16, 1024);
+            const uint64_t dv0 = smem_desc_sw128(sRing, kBlockN * 128, 1024);
+            const uint32_t dq_lo = static_cast<uint32_t>(dq), dq_hi = static_cast<uint32_t>(dq >> 32);
+            const uint32_t dk_hi = static_cast<uint32_t>(dk0 >> 32), dv_hi = static_cast<uint32_t>(dv0 >> 32);
+            constexpr uint32_t kTile16 = C::kTileBytes >> 4;
+            bool ok = mbar_wait(bars.q_full(), 0, kWaitLimitNs);
             tc_fence_after();
-            int it = 0, prev_v = -1;
+            int it = 0;
+            uint32_t prev_v_lo = 0;
+            int prev_v = -1;
             for (int j = 0; j < n_kv && ok; ++j) {
                 const int kslot = it % C::kStages, kuse = it / C::kStages;
                 ++it;
@@ -196,26 +205,23 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 ++it;
                 if (!(ok = mbar_wait(bars.full(kslot), kuse & 1, kWaitLimitNs))) break;
                 tc_fence_after();
-                const uint32_t kaddr = sRing + kslot * C::kTileBytes;
+                const uint32_t dk_lo = static_cast<uint32_t>(dk0) + kslot * kTile16;
                 for (int t = 0; t < kQTiles && ok; ++t) {
                     if (j > 0) {
-                        if (!(ok = mbar_wait(bars.p_full[t], (j - 1) & 1, kWaitLimitNs))) break;
+                        if (!(ok = mbar_wait(bars.p_full(t), (j - 1) & 1, kWaitLimitNs))) break;
                         tc_fence_after();
-                        const uint32_t vaddr = sRing + prev_v * C::kTileBytes;
 #pragma unroll
                         for (int kk = 0; kk < kBlockN / 16; ++kk)
-                            mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
-                                   smem_desc_sw128(vaddr + kk * 16 * 128, kBlockN * 128, 1024), idO,
-                                   (j > 1 || kk > 0) ? 1u : 0u);
+                            mma_ts_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + kk * 128, dv_hi,
+                                        idO, (j > 1 || kk > 0) ? 1u : 0u);
                     }
-                    const uint32_t qaddr = sQ + t * C::kTileBytes;
+                    const uint32_t aq_lo = dq_lo + t * kTile16;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t koff = (kk / 4) * 16384 + (kk % 4) * 32;
-                        mma_ss(tmem + t * 128, smem_desc_sw128(qaddr + koff, 16, 1024),
-                               smem_desc_sw128(kaddr + koff, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                        const uint32_t koff = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+                        mma_ss_lohi(tmem + t * 128, aq_lo + koff, dq_hi, dk_lo + koff, dk_hi, idS, kk > 0 ? 1u : 0u);
                     }
-                    mma_commit(bars.s_full[t]);
+                    mma_commit(bars.s_full(t));
                 }
                 if (!ok) break;
                 mma_commit(bars.empty(kslot));
@@ -223,23 +229,22 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (!(ok = mbar_wait(bars.full(vslot), vuse & 1, kWaitLimitNs))) break;
                 tc_fence_after();
                 prev_v = vslot;
+                prev_v_lo = static_cast<uint32_t>(dv0) + vslot * kTile16;
             }
             for (int t = 0; t < kQTiles && ok; ++t) {
-                if (!(ok = mbar_wait(bars.p_full[t], (n_kv - 1) & 1, kWaitLimitNs))) break;
+                if (!(ok = mbar_wait(bars.p_full(t), (n_kv - 1) & 1, kWaitLimitNs))) break;
                 tc_fence_after();
-                const uint32_t vaddr = sRing + prev_v * C::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 16; ++kk)
-                    mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
-                           smem_desc_sw128(vaddr + kk * 16 * 128, kBlockN * 128, 1024), idO,
-                           (n_kv > 1 || kk > 0) ? 1u : 0u);
-                mma_commit(bars.o_full[t]);
+                    mma_ts_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + kk * 128, dv_hi, idO,
+                                (n_kv > 1 || kk > 0) ? 1u : 0u);
+                mma_commit(bars.o_full(t));
             }
             if (ok) mma_commit(bars.empty(prev_v));
             if (!ok) report_timeout();
             // no MMA of this CTA may still be running when tensor memory is freed
-            mma_commit(bars.mma_done);
-            mbar_wait(bars.mma_done, 0, ok ? kWaitLimitNs : kCleanupLimitNs);
+            mma_commit(bars.mma_done());
+            mbar_wait(bars.mma_done(), 0, ok ? kWaitLimitNs : kCleanupLimitNs);
         }
     } else {
         // --------------------------------------------------------------- softmax
@@ -254,7 +259,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         float lr = 0.f;           // the same sum over the bf16-rounded terms the MMA sees (normalises O)
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
-            if (!mbar_wait(bars.s_full[t], j & 1, kWaitLimitNs)) {
+            if (!mbar_wait(bars.s_full(t), j & 1, kWaitLimitNs)) {
                 ok = false;
                 break;
             }
@@ -278,33 +283,48 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 for (int i = 0; i < kBlockN; ++i)
                     if (k0 + i > lim) s[i] = -INFINITY;
             }
-            float mt = s[0];
+            // row max: eight independent chains of 3-input maxes
+            float mx[8];
 #pragma unroll
-            for (int i = 1; i < kBlockN; ++i) mt = fmaxf(mt, s[i]);
+            for (int g = 0; g < 8; ++g) {
+                const int b = 16 * g;
+                float a = fmax3(s[b], s[b + 1], s[b + 2]);
+#pragma unroll
+                for (int i = 3; i < 15; i += 2) a = fmax3(a, s[b + i], s[b + i + 1]);
+                mx[g] = fmaxf(a, s[b + 15]);
+            }
+            const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
             const float m_new = fmaxf(m_ref, mt);
             const bool need = (m_new - m_ref) * scale_log2 > kRescaleLog2;  // true while m_ref = -inf
             float alpha = 1.f;
             if (need) {
                 alpha = ex2((m_ref - m_new) * scale_log2);  // 0 on the first tile
                 m_ref = m_new;
-                l *= alpha;
-                lr *= alpha;
             }
-            // P = exp2(s * scale * log2 e - m_ref * scale * log2 e), bf16, over the first 64 columns of S_t
+            // P = exp2(s * scale * log2 e - m_ref * scale * log2 e), bf16, over the first 64 columns of S_t;
+            // fp32 and bf16-rounded row sums in independent partial accumulators
             const float mc = (m_ref == -INFINITY ? 0.f : m_ref) * scale_log2;
+            const float2 c2 = make_float2(scale_log2, scale_log2), nmc2 = make_float2(-mc, -mc);
+            float2 lf[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                            make_float2(0.f, 0.f)};
+            float lq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t p[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2(fmaf(s[c * 32 + 2 * i], scale_log2, -mc));
-                    const float p1 = ex2(fmaf(s[c * 32 + 2 * i + 1], scale_log2, -mc));
-                    l += p0 + p1;
+                    const float2 x = fma2(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), c2, nmc2);
+                    const float p0 = ex2(x.x), p1 = ex2(x.y);
+                    lf[i & 3] = add2(lf[i & 3], make_float2(p0, p1));
                     p[i] = pack_bf16x2(p0, p1);
-                    lr += __uint_as_float(p[i] << 16) + __uint_as_float(p[i] & 0xffff0000u);
+                    lq[i & 3] = add_bf16x2(lq[i & 3], p[i]);
                 }
                 tmem_st16(tS + c * 16, p);
             }
+            const float2 lf01 = add2(lf[0], lf[1]), lf23 = add2(lf[2], lf[3]);
+            const float2 lfs = add2(lf01, lf23);
+            l = l * alpha + (lfs.x + lfs.y);
+            lr = lr * alpha + ((lq[0] + lq[1]) + (lq[2] + lq[3]));
             // numerator rescale u *= alpha (u holds P V up to tile j-1, complete: the
             // commit that signalled S_t(j) was issued after that MMA); nothing to scale at j = 0
             if (j > 0 && __any_sync(0xffffffffu, need)) {
@@ -314,15 +334,21 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     tmem_ld32(tO + c * 32, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                    for (int i = 0; i < 32; i += 2) {
+                        const float2 y = mul2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                              make_float2(alpha, alpha));
+                        r[i] = __float_as_uint(y.x);
+                        r[i + 1] = __float_as_uint(y.y);
+                    }
                     tmem_st32(tO + c * 32, r);
                 }
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bars.p_full[t]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.p_full(t));
         }
-        if (ok) ok = mbar_wait(bars.o_full[t], 0, kWaitLimitNs);
+        if (ok) ok = mbar_wait(bars.o_full(t), 0, kWaitLimitNs);
         if (!ok) report_timeout();
         tc_fence_after();
         // epilogue: O = u / l in bf16, staged (128-byte swizzle) in this tile's Q buffer.
