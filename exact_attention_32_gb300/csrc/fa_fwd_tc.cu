@@ -6,8 +6,11 @@
 // ("6.1 FlashAttention V1 in detail", sections 1.1 and 5.1; LSE as in
 // "FlashAttention: IO-Aware Tiling, ...", section "Backward Pass Recomputation").
 //
-// How: each CTA owns 2 query tiles of 128 rows (256 consecutive rows of one
-// (b, h) slice) and streams the admitted 128-key K/V tiles once for both.
+// How: a work unit is 2 query tiles of 128 rows (256 consecutive rows of one
+// (b, h) slice) that share one stream of the admitted 128-key K/V tiles.  The
+// grid is persistent (one CTA per SM); each CTA walks its units longest-first,
+// with barrier phases carried across units so that the next unit's Q and K/V
+// loads and first S MMAs overlap the current unit's last P V and epilogue.
 // Per K/V tile j and query tile t the running statistics are merged as in
 // "FlashAttention: optimize data movement before counting FLOPs", section 02
 // (m' = max(m, max s), l' = e^(m-m') l + sum e^(s-m'), u' = e^(m-m') u + P V):
@@ -17,7 +20,8 @@
 // Roles (320 threads):
 //   warps 0-3  softmax warpgroup of query tile 0 (one thread per row)
 //   warps 4-7  softmax warpgroup of query tile 1
-//   warp  8    TMA producer: Q tiles once, then K_j, V_j into a ring of slots
+//   warp  8    TMA producer: per unit the Q tiles (once the previous unit's last
+//              S MMAs are done), then K_j, V_j into a ring of slots
 //   warp  9    tcgen05 issuer (and TMEM owner):
 //                S_t  = Q_t K_j^T          (A, B from shared memory)
 //                O_t += P_t V_j            (A = P from tensor memory)
@@ -33,6 +37,9 @@
 // exponentials stay in range; LSE = m_ref + ln(l) holds for any reference).
 // Keys >= N and, when causal, keys j > i are set to -inf before the max
 // ("6.1 ...", section 8.3: the K/V out-of-range mask).
+//
+// The epilogue (O / l to bf16, LSE) writes straight from registers to global
+// memory, one row per thread; rows past N are not written.
 //
 // Every mbarrier wait is bounded; a wait that gives up sets FA_ERR_TIMEOUT in
 // a device status word and the CTA winds down (waiting, bounded, for its own
@@ -70,58 +77,78 @@ struct Cfg {
     static constexpr int kAtoms = D / 64;               // 128-byte-wide column blocks per tile
     static constexpr int kStages = D == 128 ? 4 : 8;    // K/V ring slots
     static constexpr int kBarOffset = (kQTiles + kStages) * kTileBytes;
-    // barriers: q_full, s_full[2], p_full[2], o_full[2], mma_done, kv_full[S], kv_empty[S]
-    static constexpr int kNumBars = 8 + 2 * kStages;
+    // barriers: q_full, q_empty, s_full[2], p_full[2], o_full[2], mma_done, kv_full[S], kv_empty[S]
+    static constexpr int kNumBars = 9 + 2 * kStages;
     static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
 };
 
-// Shared-memory addresses of the mbarriers, laid out from `base`:
-// q_full, s_full[2], p_full[2], o_full[2], mma_done, kv_full[S], kv_empty[S].
+// Shared-memory addresses of the mbarriers, laid out from `base`: q_full,
+// q_empty, s_full[2], p_full[2], o_full[2], mma_done, kv_full[S], kv_empty[S].
 template <int STAGES>
 struct Bars {
     uint32_t base;
     __device__ uint32_t q_full() const { return base; }
-    __device__ uint32_t s_full(int t) const { return base + 8u + 8u * t; }
-    __device__ uint32_t p_full(int t) const { return base + 24u + 8u * t; }
-    __device__ uint32_t o_full(int t) const { return base + 40u + 8u * t; }
-    __device__ uint32_t mma_done() const { return base + 56u; }
-    __device__ uint32_t full(int s) const { return base + 64u + 8u * s; }
-    __device__ uint32_t empty(int s) const { return base + 64u + 8u * (STAGES + s); }
+    __device__ uint32_t q_empty() const { return base + 8u; }
+    __device__ uint32_t s_full(int t) const { return base + 16u + 8u * t; }
+    __device__ uint32_t p_full(int t) const { return base + 32u + 8u * t; }
+    __device__ uint32_t o_full(int t) const { return base + 48u + 8u * t; }
+    __device__ uint32_t mma_done() const { return base + 64u; }
+    __device__ uint32_t full(int s) const { return base + 72u + 8u * s; }
+    __device__ uint32_t empty(int s) const { return base + 72u + 8u * (STAGES + s); }
 };
 
 __device__ __forceinline__ void report_timeout() { atomicExch(&g_tc_status, FA_ERR_TIMEOUT); }
 
+// Work unit u: 256 consecutive query rows of one (b, h) slice.  Causal units
+// are ordered heaviest row block first.  CTA c of a persistent grid of G CTAs
+// takes, in round r, unit r*G + c when r is even and r*G + (G-1-c) when r is
+// odd: the zigzag pairs heavy units with light ones, so every CTA ends up with
+// about the same number of K/V tiles without a shared counter.
+struct Unit {
+    int bh, q_row0, n_kv;
+};
+
+__device__ __forceinline__ int unit_index(int r)
+{
+    const int G = gridDim.x, c = blockIdx.x;
+    return r * G + ((r & 1) ? (G - 1 - c) : c);
+}
+
+template <bool CAUSAL>
+__device__ __forceinline__ Unit unit_of(int u, int N, int BH, int n_mblocks)
+{
+    const int mb = CAUSAL ? (n_mblocks - 1 - u / BH) : (u / BH);
+    Unit w;
+    w.bh = u % BH;
+    w.q_row0 = mb * (kQTiles * kBlockM);
+    const int kv_end = CAUSAL ? min(N, w.q_row0 + kQTiles * kBlockM) : N;
+    w.n_kv = (kv_end + kBlockN - 1) / kBlockN;
+    return w;
+}
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                 float *__restrict__ lse, int N, int BH, int n_mblocks, float scale, float scale_log2)
+                 const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ o, float *__restrict__ lse,
+                 int N, int BH, int n_mblocks, int n_units, float scale, float scale_log2)
 {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s_base = smem_u32(smem);
-    const uint32_t sQ = s_base;                         // kQTiles tiles
+    const uint32_t sQ = s_base;  // kQTiles tiles
     const uint32_t sRing = s_base + kQTiles * C::kTileBytes;
     const uint32_t bar0 = s_base + C::kBarOffset;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kBarOffset + C::kNumBars * 8);
 
     const Bars<C::kStages> bars{bar0};
-
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    // work unit: 256 query rows of one (b, h); causal: heaviest row blocks first
-    const int unit = blockIdx.x;
-    const int mb = CAUSAL ? (n_mblocks - 1 - unit / BH) : (unit / BH);
-    const int bh = unit % BH;
-    const int q_row0 = mb * (kQTiles * kBlockM);
-    const int kv_end = CAUSAL ? min(N, q_row0 + kQTiles * kBlockM) : N;
-    const int n_kv = (kv_end + kBlockN - 1) / kBlockN;
     // after a timeout anywhere (sticky until read by the host) CTAs do no work
-    const bool run = n_kv > 0 && *reinterpret_cast<volatile int *>(&g_tc_status) == 0;
+    const bool run = *reinterpret_cast<volatile int *>(&g_tc_status) == 0;
 
     if (tid == 0) {
         mbar_init(bars.q_full(), 1);
+        mbar_init(bars.q_empty(), 1);
         for (int t = 0; t < 2; ++t) {
             mbar_init(bars.s_full(t), 1);
             mbar_init(bars.p_full(t), kBlockM / 32);  // one arrive per softmax warp
@@ -151,31 +178,39 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            mbar_arrive_expect_tx(bars.q_full(), kQTiles * C::kTileBytes);
-            for (int t = 0; t < kQTiles; ++t)
-                for (int a = 0; a < C::kAtoms; ++a)
-                    tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &tm_q, bars.q_full(), a * 64,
-                                q_row0 + t * kBlockM, bh);
             bool ok = true;
-            int it = 0;
-            for (int j = 0; j < n_kv && ok; ++j) {
-                for (int kind = 0; kind < 2 && ok; ++kind, ++it) {
-                    const int slot = it % C::kStages, use = it / C::kStages;
-                    if (!mbar_wait(bars.empty(slot), (use & 1) ^ 1, kWaitLimitNs)) {
-                        ok = false;
-                        report_timeout();
-                        break;
-                    }
-                    mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
-                    const CUtensorMap *tm = kind == 0 ? &tm_k : &tm_v;
-                    for (int a = 0; a < C::kAtoms; ++a)
-                        tma_load_3d(sRing + slot * C::kTileBytes + a * 16384, tm, bars.full(slot), a * 64,
-                                    j * kBlockN, bh);
+            int it = 0, uc = 0;
+            for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r), ++uc) {
+                const Unit w = unit_of<CAUSAL>(u, N, BH, n_mblocks);
+                // the Q buffers are free once the previous unit's last S MMAs have completed
+                if (!mbar_wait(bars.q_empty(), (uc & 1) ^ 1, kWaitLimitNs)) {
+                    ok = false;
+                    break;
                 }
-            }
+                mbar_arrive_expect_tx(bars.q_full(), kQTiles * C::kTileBytes);
+                for (int t = 0; t < kQTiles; ++t)
+                    for (int a = 0; a < C::kAtoms; ++a)
+                        tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &tm_q, bars.q_full(), a * 64,
+                                    w.q_row0 + t * kBlockM, w.bh);
+                for (int j = 0; j < w.n_kv && ok; ++j) {
+                    for (int kind = 0; kind < 2; ++kind, ++it) {
+                        const int slot = it % C::kStages, use = it / C::kStages;
+                        if (!mbar_wait(bars.empty(slot), (use & 1) ^ 1, kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
+                        const CUtensorMap *tm = kind == 0 ? &tm_k : &tm_v;
+                        for (int a = 0; a < C::kAtoms; ++a)
+                            tma_load_3d(sRing + slot * C::kTileBytes + a * 16384, tm, bars.full(slot), a * 64,
+                                        j * kBlockN, w.bh);
+                    }
+                }
+            }  // a ring wait that fails ends the body normally, so ++uc still counts its Q load
+            if (!ok) report_timeout();
             // every copy this thread issued has landed before the CTA may exit
             const uint64_t lim = ok ? kWaitLimitNs : kCleanupLimitNs;
-            mbar_wait(bars.q_full(), 0, lim);
+            if (uc > 0) mbar_wait(bars.q_full(), (uc - 1) & 1, lim);
             for (int k = max(0, it - C::kStages); k < it; ++k)
                 mbar_wait(bars.full(k % C::kStages), (k / C::kStages) & 1, lim);
         }
@@ -193,54 +228,61 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const uint32_t dq_lo = static_cast<uint32_t>(dq), dq_hi = static_cast<uint32_t>(dq >> 32);
             const uint32_t dk_hi = static_cast<uint32_t>(dk0 >> 32), dv_hi = static_cast<uint32_t>(dv0 >> 32);
             constexpr uint32_t kTile16 = C::kTileBytes >> 4;
-            bool ok = mbar_wait(bars.q_full(), 0, kWaitLimitNs);
-            tc_fence_after();
-            int it = 0;
-            uint32_t prev_v_lo = 0;
-            int prev_v = -1;
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int kslot = it % C::kStages, kuse = it / C::kStages;
-                ++it;
-                const int vslot = it % C::kStages, vuse = it / C::kStages;
-                ++it;
-                if (!(ok = mbar_wait(bars.full(kslot), kuse & 1, kWaitLimitNs))) break;
+            bool ok = true;
+            int it = 0, uc = 0, jg = 0;  // ring position, units done, K/V tiles done (all units)
+            for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r), ++uc) {
+                const Unit w = unit_of<CAUSAL>(u, N, BH, n_mblocks);
+                if (!(ok = mbar_wait(bars.q_full(), uc & 1, kWaitLimitNs))) break;
                 tc_fence_after();
-                const uint32_t dk_lo = static_cast<uint32_t>(dk0) + kslot * kTile16;
-                for (int t = 0; t < kQTiles && ok; ++t) {
-                    if (j > 0) {
-                        if (!(ok = mbar_wait(bars.p_full(t), (j - 1) & 1, kWaitLimitNs))) break;
-                        tc_fence_after();
+                uint32_t prev_v_lo = 0;
+                int prev_v = -1;
+                for (int j = 0; j < w.n_kv && ok; ++j, ++jg) {
+                    const int kslot = it % C::kStages, kuse = it / C::kStages;
+                    ++it;
+                    const int vslot = it % C::kStages, vuse = it / C::kStages;
+                    ++it;
+                    if (!(ok = mbar_wait(bars.full(kslot), kuse & 1, kWaitLimitNs))) break;
+                    tc_fence_after();
+                    const uint32_t dk_lo = static_cast<uint32_t>(dk0) + kslot * kTile16;
+                    for (int t = 0; t < kQTiles && ok; ++t) {
+                        if (j > 0) {
+                            if (!(ok = mbar_wait(bars.p_full(t), (jg - 1) & 1, kWaitLimitNs))) break;
+                            tc_fence_after();
 #pragma unroll
-                        for (int kk = 0; kk < kBlockN / 16; ++kk)
-                            mma_ts_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + kk * 128, dv_hi,
-                                        idO, (j > 1 || kk > 0) ? 1u : 0u);
-                    }
-                    const uint32_t aq_lo = dq_lo + t * kTile16;
+                            for (int kk = 0; kk < kBlockN / 16; ++kk)
+                                mma_ts_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + kk * 128,
+                                            dv_hi, idO, (j > 1 || kk > 0) ? 1u : 0u);
+                        }
+                        const uint32_t aq_lo = dq_lo + t * kTile16;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t koff = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
-                        mma_ss_lohi(tmem + t * 128, aq_lo + koff, dq_hi, dk_lo + koff, dk_hi, idS, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t koff = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+                            mma_ss_lohi(tmem + t * 128, aq_lo + koff, dq_hi, dk_lo + koff, dk_hi, idS,
+                                        kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(bars.s_full(t));
                     }
-                    mma_commit(bars.s_full(t));
+                    if (!ok) break;
+                    mma_commit(bars.empty(kslot));
+                    if (j > 0) mma_commit(bars.empty(prev_v));
+                    if (!(ok = mbar_wait(bars.full(vslot), vuse & 1, kWaitLimitNs))) break;
+                    tc_fence_after();
+                    prev_v = vslot;
+                    prev_v_lo = static_cast<uint32_t>(dv0) + vslot * kTile16;
                 }
                 if (!ok) break;
-                mma_commit(bars.empty(kslot));
-                if (j > 0) mma_commit(bars.empty(prev_v));
-                if (!(ok = mbar_wait(bars.full(vslot), vuse & 1, kWaitLimitNs))) break;
-                tc_fence_after();
-                prev_v = vslot;
-                prev_v_lo = static_cast<uint32_t>(dv0) + vslot * kTile16;
-            }
-            for (int t = 0; t < kQTiles && ok; ++t) {
-                if (!(ok = mbar_wait(bars.p_full(t), (n_kv - 1) & 1, kWaitLimitNs))) break;
-                tc_fence_after();
+                mma_commit(bars.q_empty());  // the last reads of this unit's Q are issued
+                for (int t = 0; t < kQTiles && ok; ++t) {
+                    if (!(ok = mbar_wait(bars.p_full(t), (jg - 1) & 1, kWaitLimitNs))) break;
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk)
-                    mma_ts_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + kk * 128, dv_hi, idO,
-                                (n_kv > 1 || kk > 0) ? 1u : 0u);
-                mma_commit(bars.o_full(t));
+                    for (int kk = 0; kk < kBlockN / 16; ++kk)
+                        mma_ts_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + kk * 128, dv_hi,
+                                    idO, (w.n_kv > 1 || kk > 0) ? 1u : 0u);
+                    mma_commit(bars.o_full(t));
+                }
+                if (ok) mma_commit(bars.empty(prev_v));
             }
-            if (ok) mma_commit(bars.empty(prev_v));
             if (!ok) report_timeout();
             // no MMA of this CTA may still be running when tensor memory is freed
             mma_commit(bars.mma_done());
@@ -248,141 +290,141 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
     } else {
         // --------------------------------------------------------------- softmax
-        const int t = warp >> 2;          // query tile of this warpgroup
-        const int row = tid & 127;        // row within the tile == TMEM lane
-        const int row_g = q_row0 + t * kBlockM + row;
+        const int t = warp >> 2;    // query tile of this warpgroup
+        const int row = tid & 127;  // row within the tile == TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_off + t * 128;
         const uint32_t tO = tmem + lane_off + 256 + t * 128;
-        float m_ref = -INFINITY;  // reference max, unscaled units
-        float l = 0.f;            // exp-sum relative to m_ref (fp32 terms; gives LSE)
-        float lr = 0.f;           // the same sum over the bf16-rounded terms the MMA sees (normalises O)
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            if (!mbar_wait(bars.s_full(t), j & 1, kWaitLimitNs)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            float s[kBlockN];
-            {
-                uint32_t r[4][32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, r[c]);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
-            }
-            const int k0 = j * kBlockN;
-            const bool need_mask = (k0 + kBlockN > N) || (CAUSAL && k0 + kBlockN - 1 > q_row0 + t * kBlockM);
-            if (need_mask) {
-                const int lim = CAUSAL ? min(N - 1, row_g) : N - 1;  // last admitted key
-#pragma unroll
-                for (int i = 0; i < kBlockN; ++i)
-                    if (k0 + i > lim) s[i] = -INFINITY;
-            }
-            // row max: eight independent chains of 3-input maxes
-            float mx[8];
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                const int b = 16 * g;
-                float a = fmax3(s[b], s[b + 1], s[b + 2]);
-#pragma unroll
-                for (int i = 3; i < 15; i += 2) a = fmax3(a, s[b + i], s[b + i + 1]);
-                mx[g] = fmaxf(a, s[b + 15]);
-            }
-            const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-            const float m_new = fmaxf(m_ref, mt);
-            const bool need = (m_new - m_ref) * scale_log2 > kRescaleLog2;  // true while m_ref = -inf
-            float alpha = 1.f;
-            if (need) {
-                alpha = ex2((m_ref - m_new) * scale_log2);  // 0 on the first tile
-                m_ref = m_new;
-            }
-            // P = exp2(s * scale * log2 e - m_ref * scale * log2 e), bf16, over the first 64 columns of S_t;
-            // fp32 and bf16-rounded row sums in independent partial accumulators
-            const float mc = (m_ref == -INFINITY ? 0.f : m_ref) * scale_log2;
-            const float2 c2 = make_float2(scale_log2, scale_log2), nmc2 = make_float2(-mc, -mc);
-            float2 lf[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                            make_float2(0.f, 0.f)};
-            float lq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t p[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float2 x = fma2(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), c2, nmc2);
-                    const float p0 = ex2(x.x), p1 = ex2(x.y);
-                    lf[i & 3] = add2(lf[i & 3], make_float2(p0, p1));
-                    p[i] = pack_bf16x2(p0, p1);
-                    lq[i & 3] = add_bf16x2(lq[i & 3], p[i]);
+        int jg = 0, uc = 0;
+        for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r), ++uc) {
+            const Unit w = unit_of<CAUSAL>(u, N, BH, n_mblocks);
+            const int row_g = w.q_row0 + t * kBlockM + row;
+            float m_ref = -INFINITY;  // reference max, unscaled units
+            float l = 0.f;            // exp-sum relative to m_ref (fp32 terms; gives LSE)
+            float lr = 0.f;           // the same sum over the bf16-rounded terms the MMA sees (normalises O)
+            for (int j = 0; j < w.n_kv; ++j, ++jg) {
+                if (!mbar_wait(bars.s_full(t), jg & 1, kWaitLimitNs)) {
+                    ok = false;
+                    break;
                 }
-                tmem_st16(tS + c * 16, p);
-            }
-            const float2 lf01 = add2(lf[0], lf[1]), lf23 = add2(lf[2], lf[3]);
-            const float2 lfs = add2(lf01, lf23);
-            l = l * alpha + (lfs.x + lfs.y);
-            lr = lr * alpha + ((lq[0] + lq[1]) + (lq[2] + lq[3]));
-            // numerator rescale u *= alpha (u holds P V up to tile j-1, complete: the
-            // commit that signalled S_t(j) was issued after that MMA); nothing to scale at j = 0
-            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                tc_fence_after();
+                float s[kBlockN];
+                {
+                    uint32_t r[4][32];
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(tO + c * 32, r);
+                    for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, r[c]);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const float2 y = mul2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
-                                              make_float2(alpha, alpha));
-                        r[i] = __float_as_uint(y.x);
-                        r[i + 1] = __float_as_uint(y.y);
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
+                }
+                const int k0 = j * kBlockN;
+                const bool need_mask =
+                    (k0 + kBlockN > N) || (CAUSAL && k0 + kBlockN - 1 > w.q_row0 + t * kBlockM);
+                if (need_mask) {
+                    const int lim = CAUSAL ? min(N - 1, row_g) : N - 1;  // last admitted key
+#pragma unroll
+                    for (int i = 0; i < kBlockN; ++i)
+                        if (k0 + i > lim) s[i] = -INFINITY;
+                }
+                // row max: eight independent chains of 3-input maxes
+                float mx[8];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    const int b = 16 * g;
+                    float a = fmax3(s[b], s[b + 1], s[b + 2]);
+#pragma unroll
+                    for (int i = 3; i < 15; i += 2) a = fmax3(a, s[b + i], s[b + i + 1]);
+                    mx[g] = fmaxf(a, s[b + 15]);
+                }
+                const float mt =
+                    fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+                const float m_new = fmaxf(m_ref, mt);
+                const bool need = (m_new - m_ref) * scale_log2 > kRescaleLog2;  // true while m_ref = -inf
+                float alpha = 1.f;
+                if (need) {
+                    alpha = ex2((m_ref - m_new) * scale_log2);  // 0 on the first tile
+                    m_ref = m_new;
+                }
+                // P = exp2(s * scale * log2 e - m_ref * scale * log2 e), bf16, over the first 64 columns
+                // of S_t; fp32 and bf16-rounded row sums in independent partial accumulators
+                const float mc = (m_ref == -INFINITY ? 0.f : m_ref) * scale_log2;
+                const float2 c2 = make_float2(scale_log2, scale_log2), nmc2 = make_float2(-mc, -mc);
+                float2 lf[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                make_float2(0.f, 0.f)};
+                float lq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t p[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 x = fma2(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), c2, nmc2);
+                        const float p0 = ex2(x.x), p1 = ex2(x.y);
+                        lf[i & 3] = add2(lf[i & 3], make_float2(p0, p1));
+                        p[i] = pack_bf16x2(p0, p1);
+                        lq[i & 3] = add_bf16x2(lq[i & 3], p[i]);
                     }
-                    tmem_st32(tO + c * 32, r);
+                    tmem_st16(tS + c * 16, p);
+                }
+                const float2 lf01 = add2(lf[0], lf[1]), lf23 = add2(lf[2], lf[3]);
+                const float2 lfs = add2(lf01, lf23);
+                l = l * alpha + (lfs.x + lfs.y);
+                lr = lr * alpha + ((lq[0] + lq[1]) + (lq[2] + lq[3]));
+                // numerator rescale u *= alpha (u holds P V up to tile j-1, complete: the
+                // commit that signalled S_t(j) was issued after that MMA); nothing to scale at j = 0
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(tO + c * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const float2 y = mul2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                                  make_float2(alpha, alpha));
+                            r[i] = __float_as_uint(y.x);
+                            r[i + 1] = __float_as_uint(y.y);
+                        }
+                        tmem_st32(tO + c * 32, r);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.p_full(t));
+            }
+            if (!ok || !(ok = mbar_wait(bars.o_full(t), uc & 1, kWaitLimitNs))) break;
+            tc_fence_after();
+            // epilogue: O = u / l in bf16 straight from registers to global memory.
+            // u was accumulated from bf16-rounded P, so it is divided by the sum of
+            // those same rounded terms: the weights then sum to one exactly and a
+            // row dominated by one key returns that key's value without a P-rounding
+            // error.  The next unit's first P V (which overwrites O_t) is issued
+            // only after this warpgroup's next p_full arrive, so the reads here are safe.
+            const float inv_l = 1.f / lr;
+            __nv_bfloat16 *orow = o + (static_cast<int64_t>(w.bh) * N + row_g) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tO + c * 32, r);
+                tmem_wait_ld();
+                if (row_g < N) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(r[q4 * 8 + 0]) * inv_l, __uint_as_float(r[q4 * 8 + 1]) * inv_l);
+                        v.y = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2]) * inv_l, __uint_as_float(r[q4 * 8 + 3]) * inv_l);
+                        v.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * inv_l, __uint_as_float(r[q4 * 8 + 5]) * inv_l);
+                        v.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * inv_l, __uint_as_float(r[q4 * 8 + 7]) * inv_l);
+                        *reinterpret_cast<uint4 *>(orow + c * 32 + q4 * 8) = v;
+                    }
                 }
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.p_full(t));
+            if (row_g < N) lse[static_cast<int64_t>(w.bh) * N + row_g] = m_ref * scale + logf(l);
         }
-        if (ok) ok = mbar_wait(bars.o_full(t), 0, kWaitLimitNs);
         if (!ok) report_timeout();
-        tc_fence_after();
-        // epilogue: O = u / l in bf16, staged (128-byte swizzle) in this tile's Q buffer.
-        // u was accumulated from bf16-rounded P, so it is divided by the sum of
-        // those same rounded terms: the weights then sum to one exactly and a
-        // row dominated by one key returns that key's value without a P-rounding error.
-        const float inv_l = 1.f / lr;
-        uint8_t *stage = smem + t * C::kTileBytes;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tO + c * 32, r);
-            tmem_wait_ld();
-            const int a = c / 2;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const int chunk = (c % 2) * 4 + q4;
-                uint4 v;
-                v.x = pack_bf16x2(__uint_as_float(r[q4 * 8 + 0]) * inv_l, __uint_as_float(r[q4 * 8 + 1]) * inv_l);
-                v.y = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2]) * inv_l, __uint_as_float(r[q4 * 8 + 3]) * inv_l);
-                v.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * inv_l, __uint_as_float(r[q4 * 8 + 5]) * inv_l);
-                v.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * inv_l, __uint_as_float(r[q4 * 8 + 7]) * inv_l);
-                *reinterpret_cast<uint4 *>(stage + a * 16384 + row * 128 + ((chunk ^ (row & 7)) * 16)) = v;
-            }
-        }
-        if (row_g < N && ok) lse[static_cast<int64_t>(bh) * N + row_g] = m_ref * scale + logf(l);
-        fence_proxy_async_smem();
-        named_bar_sync(1 + t, kBlockM);
-        if (row == 0 && ok && q_row0 + t * kBlockM < N) {
-            for (int a = 0; a < C::kAtoms; ++a)
-                tma_store_3d(&tm_o, smem_u32(stage) + a * 16384, a * 64, q_row0 + t * kBlockM, bh);
-            bulk_commit();
-            bulk_wait0();
-        }
     }
     tc_fence_before();
     __syncthreads();
@@ -433,21 +475,21 @@ template <int D, bool CAUSAL>
 cudaError_t launch(const FaProblem &p, cudaStream_t stream)
 {
     using C = Cfg<D>;
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     const int64_t BH = p.B * p.H;
-    if (!make_map(&mq, p.q, BH, p.N, D) || !make_map(&mk, p.k, BH, p.N, D) || !make_map(&mv, p.v, BH, p.N, D) ||
-        !make_map(&mo, p.o, BH, p.N, D))
+    if (!make_map(&mq, p.q, BH, p.N, D) || !make_map(&mk, p.k, BH, p.N, D) || !make_map(&mv, p.v, BH, p.N, D))
         return cudaErrorInvalidValue;
     auto kern = fa_fwd_tc_kernel<D, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t n_mblocks = (p.N + kQTiles * kBlockM - 1) / (kQTiles * kBlockM);
-    const int64_t blocks = n_mblocks * BH;
-    if (blocks > 0x7fffffffLL || BH > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const int64_t n_units = n_mblocks * BH;
+    if (n_units > 0x7fffffffLL || BH > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const int64_t grid = n_units < p.sm_count ? n_units : p.sm_count;  // persistent: one CTA per SM
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
-    kern<<<static_cast<unsigned>(blocks), kThreads, C::kSmemBytes, stream>>>(
-        mq, mk, mv, mo, p.lse, static_cast<int>(p.N), static_cast<int>(BH), static_cast<int>(n_mblocks), p.scale,
-        scale_log2);
+    kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
+        mq, mk, mv, static_cast<__nv_bfloat16 *>(p.o), p.lse, static_cast<int>(p.N), static_cast<int>(BH),
+        static_cast<int>(n_mblocks), static_cast<int>(n_units), p.scale, scale_log2);
     return cudaGetLastError();
 }
 

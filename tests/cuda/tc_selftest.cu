@@ -140,3 +140,32 @@ extern "C" int tc_selftest(const void *q, const void *k, const void *v, float *s
     e = cudaDeviceSynchronize();
     return static_cast<int>(e);
 }
+
+// A bounded wait that must run out: an mbarrier expecting one arrival that
+// never comes.  The waiting thread gives up after `limit_ns` and records 1 in
+// status[0]; a wait for the phase before the current one (parity 1 on a fresh
+// barrier) must succeed at once and records 1 in status[1].
+__global__ void wait_timeout_kernel(int *status, unsigned long long limit_ns, unsigned long long *elapsed_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        status[1] = mbar_wait(smem_u32(&bar), 1, limit_ns) ? 1 : 0;
+        const uint64_t t0 = globaltimer_ns();
+        const bool ok = mbar_wait(smem_u32(&bar), 0, limit_ns);
+        *elapsed_ns = globaltimer_ns() - t0;
+        status[0] = ok ? 0 : 1;
+    }
+}
+
+extern "C" int wait_timeout_selftest(int *status, unsigned long long limit_ns, unsigned long long *elapsed_ns)
+{
+    wait_timeout_kernel<<<1, 32>>>(status, limit_ns, elapsed_ns);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    return static_cast<int>(e);
+}

@@ -131,3 +131,16 @@ def test_runs_on_a_side_stream():
     s.synchronize()
     o_ref, lse_ref = oracle.attention(q, k, v, 0.125, False)
     check(o.double().cpu().numpy(), lse.double().cpu().numpy(), o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("d,causal", [(64, True), (128, False), (128, True)])
+def test_many_work_units_per_cta(d, causal, kernel):
+    # 8 x 64 slices of 300 rows: about seven 256-row work units per SM, so each
+    # persistent CTA carries its pipeline state (barrier phases, ring position)
+    # across units of different lengths; every row is compared
+    q, k, v = make_inputs(8, 64, 300, d, seed=900 + d + causal)
+    scale = float(np.float32(1 / np.sqrt(d)))
+    o, lse = run_gpu(q, k, v, scale, causal, kernel)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, causal)
+    check(o, lse, o_ref, lse_ref)

@@ -1,4 +1,6 @@
-"""tcgen05 operand layouts the attention kernel relies on, checked bit-exactly
+"""Device building blocks of the attention kernel.
+
+tcgen05 operand layouts the attention kernel relies on, checked bit-exactly
 on small-integer data (every product and sum is exact in fp32):
 S = Q K^T with both operands K-major and 128-byte swizzled in shared memory,
 then P = bf16(S) written into tensor memory over S, and O = P V with P read
@@ -28,6 +30,8 @@ def selftest_lib():
     lib = ctypes.CDLL(so)
     lib.tc_selftest.restype = ctypes.c_int
     lib.tc_selftest.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_int]
+    lib.wait_timeout_selftest.restype = ctypes.c_int
+    lib.wait_timeout_selftest.argtypes = [ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_void_p]
     return lib
 
 
@@ -50,3 +54,18 @@ def test_mma_layouts_bit_exact(selftest_lib, d):
     p = s_ref.float().to(torch.bfloat16).double()
     o_ref = p @ v.double()
     assert torch.equal(o_out.cpu().double(), o_ref), "O = P V layout mismatch"
+
+
+def test_bounded_wait_gives_up_and_context_survives(selftest_lib):
+    # the same bounded mbarrier wait every pipeline stage of the kernel uses:
+    # nothing arrives, so it must return "timed out" after about its limit,
+    # and the CUDA context must stay usable afterwards
+    status = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    elapsed = torch.zeros(1, dtype=torch.int64, device="cuda")
+    limit_ns = 50_000_000
+    rc = selftest_lib.wait_timeout_selftest(status.data_ptr(), limit_ns, elapsed.data_ptr())
+    assert rc == 0
+    assert status.tolist() == [1, 1]  # timed out; the previous-phase wait passed at once
+    assert limit_ns <= int(elapsed.item()) < 20 * limit_ns
+    x = torch.arange(1000, device="cuda", dtype=torch.float32)
+    assert float(x.sum().item()) == 499500.0
