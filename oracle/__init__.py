@@ -5,7 +5,7 @@ benchmark's CPU-baseline leg (and its ``--impl reference`` arm) may import this
 package.  It shares no code with the CUDA path and never calls it; the CUDA
 path never calls it either.
 
-Three independent references, each in fp64 or better:
+Independent references, each in fp64 or better:
 
 ``attention``          the plain definition ("6.1 FlashAttention V1 in detail",
                        section 1.1: S = scale * Q K^T, P = softmax(S), O = P V)
@@ -20,6 +20,9 @@ Three independent references, each in fp64 or better:
                        u' = e^(m-m') u + sum e^(s-m') V; output u'/l'), in numpy
                        fp64, with any tile sizes and any K/V-tile visiting order.
                        It exists to pin the online reasoning, not the GPU.
+``merge``              the two-block merge of "FlashAttention: IO-Aware Tiling,
+                       ...", section "Online Softmax Mathematics", folding
+                       partial (O, LSE) results over disjoint key ranges.
 ``attention_decimal``  brute force in Python ``decimal`` at 50 digits, using
                        the softmax definition directly (exp(s_j) / sum exp(s_k),
                        no max shift) - an independent formulation for tiny
@@ -78,7 +81,8 @@ def _load():
             ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_double, ctypes.c_int,
             ctypes.c_void_p, ctypes.c_int64,
-            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+            ctypes.c_int64, ctypes.c_int64]
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -103,12 +107,14 @@ def _as_f64(t) -> np.ndarray:
     return t.detach().cpu().to(torch.float64).numpy()
 
 
-def attention(q, k, v, scale: float, causal: bool, rows=None, threads: int = 0):
+def attention(q, k, v, scale: float, causal: bool, rows=None, threads: int = 0, kv_range=None):
     """fp64 attention of bf16 inputs by the plain definition.
 
-    q, k, v : bf16 CPU tensors [B, H, N, d]
-    rows    : None (all rows) or an int64 array of flat row ids
-              (b*H + h)*N + i
+    q, k, v  : bf16 CPU tensors [B, H, N, d]
+    rows     : None (all rows) or an int64 array of flat row ids
+               (b*H + h)*N + i
+    kv_range : None (all keys) or (lo, hi): only keys lo <= j < hi take part;
+               a row that then admits no key gets O = 0, LSE = -inf
     Returns (O, LSE) as float64 numpy arrays: [B, H, N, d] and [B, H, N] for
     all rows, else [len(rows), d] and [len(rows)].
     """
@@ -126,10 +132,11 @@ def attention(q, k, v, scale: float, causal: bool, rows=None, threads: int = 0):
         rows_ptr = rows_arr.ctypes.data
     o = np.empty((n_rows, d), dtype=np.float64)
     lse = np.empty((n_rows,), dtype=np.float64)
+    lo, hi = (0, N) if kv_range is None else (int(kv_range[0]), int(kv_range[1]))
     rc = _load().oracle_attention_rows(
         qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, B, H, N, d,
         float(scale), int(bool(causal)), rows_ptr, n_rows,
-        o.ctypes.data, lse.ctypes.data, int(threads))
+        o.ctypes.data, lse.ctypes.data, int(threads), lo, hi)
     if rc != 0:
         raise ValueError(f"oracle_attention_rows failed ({rc})")
     if rows is None:
@@ -194,6 +201,40 @@ def attention_online(q, k, v, scale: float, causal: bool, block_q: int,
             m = m_new
         o[:, :, i0:i1, :] = u / l[..., None]
         lse[:, :, i0:i1] = m + np.log(l)
+    return o, lse
+
+
+def merge(o_parts, lse_parts):
+    """Merge partial attention results over disjoint key ranges, fp64.
+
+    o_parts [S, ..., d] (each normalised over its own keys) and lse_parts
+    [S, ...] (each m_s + ln l_s).  The parts are folded in one at a time with
+    the two-block merge of "FlashAttention: IO-Aware Tiling, ...", section
+    "Online Softmax Mathematics", taking each part as (m_s, l_s, O_s) with
+    m_s = LSE_s and l_s = 1:
+        m = max(m1, m2),  l = e^(m1-m) l1 + e^(m2-m) l2,
+        O = (l1 e^(m1-m) / l) O1 + (l2 e^(m2-m) / l) O2.
+    A part with LSE = -inf (no admitted key) carries no weight.  Returns
+    (O, LSE = m + ln l).
+    """
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    m = np.full(lse_parts.shape[1:], -np.inf)
+    l = np.zeros(lse_parts.shape[1:])
+    o = np.zeros(o_parts.shape[1:])
+    for s in range(lse_parts.shape[0]):
+        m2, l2, o2 = lse_parts[s], np.where(np.isfinite(lse_parts[s]), 1.0, 0.0), o_parts[s]
+        m_new = np.maximum(m, m2)
+        ref = np.where(np.isfinite(m_new), m_new, 0.0)
+        a1 = np.where(l > 0, l * np.exp(m - ref), 0.0)
+        a2 = np.where(l2 > 0, l2 * np.exp(m2 - ref), 0.0)
+        l_new = a1 + a2
+        with np.errstate(invalid="ignore", divide="ignore"):
+            o = np.where((l_new > 0)[..., None],
+                         (a1 / l_new)[..., None] * o + (a2 / l_new)[..., None] * o2, 0.0)
+        m, l = m_new, l_new
+    with np.errstate(divide="ignore"):
+        lse = np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), -np.inf)
     return o, lse
 
 

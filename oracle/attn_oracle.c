@@ -42,21 +42,31 @@ static double widen_bf16(uint16_t bits)
 }
 
 /*
- * One query row i of one (batch, head) slice.
+ * One query row i of one (batch, head) slice, over the admitted keys j with
+ * kv_lo <= j < kv_hi (and j <= i when causal).
  *   qh, kh, vh : the slice's [N, d] row-major bf16 matrices
  *   s          : caller scratch of N doubles (the row of S)
  *   o_row      : d doubles out
  *   lse        : one double out
+ * A row that admits no key gets O = 0 and LSE = -inf (it carries no weight
+ * when partial results over disjoint key ranges are merged).
  */
 static void oracle_row(const uint16_t *qh, const uint16_t *kh, const uint16_t *vh,
                        int64_t N, int64_t d, double scale, int causal, int64_t i,
-                       double *s, double *o_row, double *lse)
+                       int64_t kv_lo, int64_t kv_hi, double *s, double *o_row, double *lse)
 {
-    const int64_t n_keys = causal ? (i + 1) : N; /* keys admitted to row i */
+    int64_t j_end = causal ? (i + 1) : N; /* keys admitted to row i: [kv_lo, j_end) */
+    if (j_end > kv_hi) j_end = kv_hi;
     const uint16_t *q = qh + i * d;
 
+    for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
+    if (j_end <= kv_lo) {
+        *lse = -INFINITY;
+        return;
+    }
+
     /* S_ij = scale * sum_c Q_ic K_jc */
-    for (int64_t j = 0; j < n_keys; ++j) {
+    for (int64_t j = kv_lo; j < j_end; ++j) {
         const uint16_t *kr = kh + j * d;
         double acc = 0.0;
         for (int64_t c = 0; c < d; ++c)
@@ -66,17 +76,16 @@ static void oracle_row(const uint16_t *qh, const uint16_t *kh, const uint16_t *v
 
     /* pass 1: m = max_j S_ij */
     double m = -INFINITY;
-    for (int64_t j = 0; j < n_keys; ++j)
+    for (int64_t j = kv_lo; j < j_end; ++j)
         if (s[j] > m) m = s[j];
 
     /* pass 2: l = sum_j exp(S_ij - m) */
     double l = 0.0;
-    for (int64_t j = 0; j < n_keys; ++j)
+    for (int64_t j = kv_lo; j < j_end; ++j)
         l += exp(s[j] - m);
 
     /* pass 3: P_ij = exp(S_ij - m) / l, then O_i = sum_j P_ij V_j */
-    for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
-    for (int64_t j = 0; j < n_keys; ++j) {
+    for (int64_t j = kv_lo; j < j_end; ++j) {
         const double p = exp(s[j] - m) / l;
         const uint16_t *vr = vh + j * d;
         for (int64_t c = 0; c < d; ++c)
@@ -95,6 +104,7 @@ static void oracle_row(const uint16_t *qh, const uint16_t *kh, const uint16_t *v
  *   o        : n_rows * d doubles out, row-major in the order of `rows`
  *   lse      : n_rows doubles out
  *   threads  : worker threads (<= 0: the OpenMP default)
+ *   kv_lo, kv_hi : only keys kv_lo <= j < kv_hi take part (0, N: all keys)
  *
  * Returns 0, or -1 on an invalid argument (nothing written).
  */
@@ -102,9 +112,12 @@ int oracle_attention_rows(const uint16_t *q, const uint16_t *k, const uint16_t *
                           int64_t B, int64_t H, int64_t N, int64_t d,
                           double scale, int causal,
                           const int64_t *rows, int64_t n_rows,
-                          double *o, double *lse, int threads)
+                          double *o, double *lse, int threads,
+                          int64_t kv_lo, int64_t kv_hi)
 {
     if (!q || !k || !v || !o || !lse || B < 1 || H < 1 || N < 1 || d < 1 || n_rows < 0)
+        return -1;
+    if (kv_lo < 0 || kv_hi > N || kv_lo >= kv_hi)
         return -1;
     if (!rows && n_rows != B * H * N)
         return -1;
@@ -131,7 +144,7 @@ int oracle_attention_rows(const uint16_t *q, const uint16_t *k, const uint16_t *
             const int64_t r = rows ? rows[t] : t;
             const int64_t bh = r / N, i = r % N;
             const int64_t base = bh * N * d;
-            oracle_row(q + base, k + base, v + base, N, d, scale, causal, i, s,
+            oracle_row(q + base, k + base, v + base, N, d, scale, causal, i, kv_lo, kv_hi, s,
                        o + t * d, lse + t);
         }
         free(s);

@@ -12,6 +12,9 @@ Each pin targets a class of mistake:
   online vs dense           - tile size / order invariance of the (m, l, u) merge
   negative test             - the K/V out-of-range mask matters
   large logits              - max subtraction keeps the result finite and exact
+  key ranges and merge      - partials over disjoint key ranges, folded with the
+                              two-block merge, give dense attention (the worked
+                              example in both orders; random splits)
 """
 import math
 import os
@@ -314,3 +317,68 @@ def test_invalid_arguments_rejected():
         oracle.attention(q, k, v, 1.0, False, rows=[4])
     with pytest.raises(ValueError):
         oracle.attention(q, k[:, :, :3], v, 1.0, False)
+
+
+# ---------------------------------------------------- key ranges and the merge
+
+@pytest.mark.parametrize("order", [[0, 1], [1, 0]])
+def test_worked_example_by_partials_and_merge(order):
+    # the page's split [2, 1] | [0] as two key ranges, merged in both orders
+    g, q, k, v = worked_example_inputs()
+    parts = [oracle.attention(q, k, v, 1.0, False, kv_range=r) for r in [(0, 2), (2, 3)]]
+    parts = [parts[i] for i in order]
+    o, lse = oracle.merge([p[0] for p in parts], [p[1] for p in parts])
+    tol = 0.5 * 10 ** -int(g["digits"][0])
+    assert np.all(np.abs(o[..., 0] - g["output"][0]) <= tol)
+    assert np.allclose(lse, 2.0 + math.log(1 + math.exp(-1) + math.exp(-2)), rtol=0, atol=1e-14)
+    # first part alone: m = 2, l = 1 + e^-1, u = 1 + 3 e^-1
+    o1, l1 = parts[order.index(0)]
+    assert np.allclose(o1[..., 0], (1 + 3 * math.exp(-1)) / (1 + math.exp(-1)), rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("cuts", [[0, 50], [0, 17, 50], [0, 1, 2, 49, 50], [0, 25, 30, 31, 50]])
+def test_merge_of_key_range_partials_is_dense(causal, cuts):
+    q, k, v = make_inputs(2, 2, 50, 8, seed=31, q_gain=3.0)
+    od, ld = oracle.attention(q, k, v, 0.4, causal)
+    parts = [oracle.attention(q, k, v, 0.4, causal, kv_range=(a, b)) for a, b in zip(cuts[:-1], cuts[1:])]
+    for perm in (list(range(len(parts))), list(range(len(parts)))[::-1]):
+        o, lse = oracle.merge([parts[i][0] for i in perm], [parts[i][1] for i in perm])
+        assert np.allclose(o, od, rtol=1e-12, atol=1e-12)
+        assert np.allclose(lse, ld, rtol=1e-13, atol=1e-12)
+
+
+def test_single_key_range_returns_that_value():
+    q, k, v = make_inputs(1, 2, 20, 8, seed=32)
+    o, lse = oracle.attention(q, k, v, 0.5, False, kv_range=(7, 8))
+    assert np.array_equal(o, np.broadcast_to(v[:, :, 7:8].to(torch.float64).numpy(), o.shape))
+    s = 0.5 * np.einsum("bhic,bhc->bhi", q.to(torch.float64).numpy(), k[:, :, 7].to(torch.float64).numpy())
+    assert np.allclose(lse, s, rtol=1e-14, atol=1e-14)
+
+
+def test_rows_without_admitted_keys():
+    # causal rows before the range start admit no key: O = 0, LSE = -inf,
+    # and such a part carries no weight in the merge
+    q, k, v = make_inputs(1, 1, 30, 4, seed=33)
+    o, lse = oracle.attention(q, k, v, 0.5, True, kv_range=(10, 30))
+    assert np.all(o[:, :, :10] == 0) and np.all(np.isneginf(lse[:, :, :10]))
+    assert np.all(np.isfinite(lse[:, :, 10:]))
+    o0, l0 = oracle.attention(q, k, v, 0.5, True, kv_range=(0, 10))
+    om, lm = oracle.merge([o0, o], [l0, lse])
+    od, ld = oracle.attention(q, k, v, 0.5, True)
+    assert np.allclose(om, od, rtol=1e-12, atol=1e-12) and np.allclose(lm, ld, rtol=1e-13, atol=1e-12)
+
+
+def test_merge_of_one_part_is_identity():
+    rng = np.random.default_rng(3)
+    o = rng.normal(size=(2, 3, 5, 4))
+    lse = rng.normal(size=(2, 3, 5)) * 10
+    om, lm = oracle.merge([o], [lse])
+    assert np.allclose(om, o, rtol=0, atol=1e-15) and np.allclose(lm, lse, rtol=0, atol=1e-14)
+
+
+def test_invalid_key_range_rejected():
+    q, k, v = make_inputs(1, 1, 4, 2, seed=1)
+    for r in [(2, 2), (-1, 3), (0, 5), (3, 1)]:
+        with pytest.raises(ValueError):
+            oracle.attention(q, k, v, 1.0, False, kv_range=r)
