@@ -23,7 +23,8 @@ _lock = threading.Lock()
 FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_NO_DEVICE",
                 4: "FA_ERR_ARCH", 5: "FA_ERR_LAUNCH", 6: "FA_ERR_TIMEOUT"}
-EXPORTED = ("fa_fwd", "fa_fwd_mma", "fa_get_device_status", "fa_status_string", "fa_version")
+EXPORTED = ("fa_fwd", "fa_fwd_mma", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_combine",
+            "fa_get_device_status", "fa_status_string", "fa_version")
 
 
 class FAError(RuntimeError):
@@ -47,6 +48,13 @@ def lib():
                                  ctypes.c_int, vp]
             L.fa_fwd_mma.restype = ctypes.c_int
             L.fa_fwd_mma.argtypes = L.fa_fwd.argtypes
+            L.fa_fwd_splitkv.restype = ctypes.c_int
+            L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
+                                         ctypes.c_int, i64, vp, i64, vp]
+            L.fa_fwd_splitkv_workspace_bytes.restype = i64
+            L.fa_fwd_splitkv_workspace_bytes.argtypes = [i64, i64, i64, i64, i64]
+            L.fa_combine.restype = ctypes.c_int
+            L.fa_combine.argtypes = [vp, vp, i64, vp, vp, i64, i64, i64, i64, vp]
             L.fa_get_device_status.restype = ctypes.c_int
             L.fa_get_device_status.argtypes = [vp]
             L.fa_status_string.restype = ctypes.c_char_p
@@ -65,6 +73,22 @@ def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
 def fa_fwd_mma(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
     """Raw call of the warp-level (mma.sync) kernel; same contract as ``fa_fwd``."""
     return lib().fa_fwd_mma(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), int(causal), stream)
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, n_splits, workspace,
+                   workspace_bytes, stream) -> int:
+    """Raw call of the split-KV forward (caller-owned workspace)."""
+    return lib().fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), int(causal),
+                                n_splits, workspace, workspace_bytes, stream)
+
+
+def fa_fwd_splitkv_workspace_bytes(B, H, N, d, n_splits) -> int:
+    return lib().fa_fwd_splitkv_workspace_bytes(B, H, N, d, n_splits)
+
+
+def fa_combine(o_parts, lse_parts, n_parts, o, lse, B, H, N, d, stream) -> int:
+    """Raw call of the merge of partial (O, LSE) results."""
+    return lib().fa_combine(o_parts, lse_parts, n_parts, o, lse, B, H, N, d, stream)
 
 
 def fa_get_device_status(stream=0) -> int:
@@ -121,3 +145,51 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | No
     if st != FA_OK:
         raise FAError(st, "fa_fwd" if kernel == "tc" else "fa_fwd_mma")
     return out, lse
+
+
+def forward_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_splits: int,
+                    scale: float | None = None, causal: bool = False,
+                    workspace: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None):
+    """O, LSE by ``fa_fwd_splitkv``; the workspace (uint8 CUDA tensor) is
+    allocated with torch when not given.  Returns (O, LSE, workspace)."""
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.shape != q.shape:
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors of one shape")
+    B, H, N, d = q.shape
+    scale = default_scale(d) if scale is None else scale
+    need = fa_fwd_splitkv_workspace_bytes(B, H, N, d, n_splits)
+    if need < 0:
+        raise FAError(1, "fa_fwd_splitkv_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        st = fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                            B, H, N, d, float(scale), bool(causal), n_splits, workspace.data_ptr(),
+                            workspace.numel() * workspace.element_size(), s.cuda_stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_splitkv")
+    return o, lse, workspace
+
+
+def combine(o_parts: torch.Tensor, lse_parts: torch.Tensor, stream: torch.cuda.Stream | None = None):
+    """Merge partial results: o_parts fp32 [S, B, H, N, d], lse_parts fp32
+    [S, B, H, N] -> (O bf16 [B, H, N, d], LSE fp32 [B, H, N]) by ``fa_combine``."""
+    if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32 or o_parts.dim() != 5:
+        raise ValueError("o_parts must be fp32 [S, B, H, N, d] and lse_parts fp32 [S, B, H, N]")
+    if not (o_parts.is_cuda and lse_parts.is_cuda and o_parts.is_contiguous() and lse_parts.is_contiguous()):
+        raise ValueError("o_parts and lse_parts must be contiguous CUDA tensors")
+    S, B, H, N, d = o_parts.shape
+    if tuple(lse_parts.shape) != (S, B, H, N):
+        raise ValueError("lse_parts must be [S, B, H, N]")
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=o_parts.device)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=o_parts.device)
+    s = stream if stream is not None else torch.cuda.current_stream(o_parts.device)
+    with torch.cuda.device(o_parts.device):
+        st = fa_combine(o_parts.data_ptr(), lse_parts.data_ptr(), S, o.data_ptr(), lse.data_ptr(),
+                        B, H, N, d, s.cuda_stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_combine")
+    return o, lse

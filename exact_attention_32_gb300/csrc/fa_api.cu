@@ -68,20 +68,45 @@ bool overlaps(const void *a, uint64_t na, const void *b, uint64_t nb)
 
 typedef cudaError_t (*Launcher)(const FaProblem &, cudaStream_t);
 
-int validate_and_launch(Launcher launch, const void *q, const void *k, const void *v, void *o, float *lse,
-                        int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal, void *stream)
+// Sizes of an attention problem; pure host logic, no CUDA call.
+int check_sizes(int64_t B, int64_t H, int64_t N, int64_t d)
 {
-    // sizes first: nothing is touched for an invalid problem
     if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
-    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-    if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
     if (N > (int64_t(1) << 31) - 256 || B > (int64_t(1) << 31) || H > (int64_t(1) << 31))
         return FA_ERR_INVALID_ARG;
     if (B * H > (int64_t(1) << 40) / N || B * H * N > (int64_t(1) << 40) / d) return FA_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+constexpr int64_t kMaxSplits = 32;
+
+// Key-split geometry of fa_fwd_splitkv: chunks of a multiple of 128 keys, no empty chunk.
+void split_geometry(int64_t N, int64_t n_splits, int64_t *chunk, int64_t *parts)
+{
+    const int64_t per = (N + n_splits - 1) / n_splits;
+    *chunk = (per + 127) / 128 * 128;
+    *parts = (N + *chunk - 1) / *chunk;
+}
+
+int64_t splitkv_bytes(int64_t B, int64_t H, int64_t N, int64_t d, int64_t n_splits)
+{
+    int64_t chunk, parts;
+    split_geometry(N, n_splits, &chunk, &parts);
+    return parts * B * H * N * (d + 1) * 4;
+}
+
+int validate_and_launch(Launcher launch, const void *q, const void *k, const void *v, void *o, float *lse,
+                        int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal, void *stream)
+{
+    // sizes first: nothing is touched for an invalid problem
+    int st = check_sizes(B, H, N, d);
+    if (st != FA_OK) return st;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
 
     int dev = 0, sm_count = 0;
-    int st = current_device(&dev, &sm_count);
+    st = current_device(&dev, &sm_count);
     if (st != FA_OK) return st;
     const void *ptrs[5] = {q, k, v, o, lse};
     for (const void *p : ptrs)
@@ -123,6 +148,91 @@ extern "C" int fa_fwd_mma(const void *q, const void *k, const void *v, void *o, 
                           int64_t H, int64_t N, int64_t d, float scale, int causal, void *stream)
 {
     return validate_and_launch(fa_launch_mma, q, k, v, o, lse, B, H, N, d, scale, causal, stream);
+}
+
+extern "C" int64_t fa_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, int64_t n_splits)
+{
+    if (check_sizes(B, H, N, d) != FA_OK || n_splits < 1 || n_splits > kMaxSplits) return -1;
+    return splitkv_bytes(B, H, N, d, n_splits);
+}
+
+extern "C" int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                              int64_t H, int64_t N, int64_t d, float scale, int causal, int64_t n_splits,
+                              void *workspace, int64_t workspace_bytes, void *stream)
+{
+    int st = check_sizes(B, H, N, d);
+    if (st != FA_OK) return st;
+    if ((causal != 0 && causal != 1) || !(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (n_splits < 1 || n_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
+    const int64_t need = splitkv_bytes(B, H, N, d, n_splits);
+    if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
+
+    int dev = 0, sm_count = 0;
+    if ((st = current_device(&dev, &sm_count)) != FA_OK) return st;
+    const void *ptrs[6] = {q, k, v, o, lse, workspace};
+    for (const void *p : ptrs)
+        if ((st = check_pointer(p, dev)) != FA_OK) return st;
+    const uint64_t tbytes = static_cast<uint64_t>(B * H * N * d) * 2u;
+    const uint64_t lbytes = static_cast<uint64_t>(B * H * N) * 4u;
+    if (overlaps(o, tbytes, lse, lbytes)) return FA_ERR_INVALID_ARG;
+    for (const void *in : {q, k, v})
+        if (overlaps(o, tbytes, in, tbytes) || overlaps(lse, lbytes, in, tbytes) ||
+            overlaps(workspace, static_cast<uint64_t>(need), in, tbytes))
+            return FA_ERR_INVALID_ARG;
+    if (overlaps(workspace, static_cast<uint64_t>(need), o, tbytes) ||
+        overlaps(workspace, static_cast<uint64_t>(need), lse, lbytes))
+        return FA_ERR_INVALID_ARG;
+
+    FaProblem p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.lse = lse;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.d = static_cast<int>(d);
+    p.scale = scale;
+    p.causal = causal;
+    p.sm_count = sm_count;
+    int64_t chunk, parts;
+    split_geometry(N, n_splits, &chunk, &parts);
+    const int64_t rows = B * H * N;
+    float *o_parts = static_cast<float *>(workspace);
+    float *lse_parts = o_parts + parts * rows * d;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (fa_launch_tc_partials(p, o_parts, lse_parts, static_cast<int>(parts), static_cast<int>(chunk), s) !=
+            cudaSuccess ||
+        fa_launch_combine(o_parts, lse_parts, static_cast<int>(parts), rows, p.d, o, lse, sm_count, s) != cudaSuccess)
+        return FA_ERR_LAUNCH;
+    return FA_OK;
+}
+
+extern "C" int fa_combine(const float *o_parts, const float *lse_parts, int64_t n_parts, void *o, float *lse,
+                          int64_t B, int64_t H, int64_t N, int64_t d, void *stream)
+{
+    int st = check_sizes(B, H, N, d);
+    if (st != FA_OK) return st;
+    if (n_parts < 1 || n_parts > kMaxSplits) return FA_ERR_INVALID_ARG;
+    int dev = 0, sm_count = 0;
+    if ((st = current_device(&dev, &sm_count)) != FA_OK) return st;
+    const void *ptrs[4] = {o_parts, lse_parts, o, lse};
+    for (const void *p : ptrs)
+        if ((st = check_pointer(p, dev)) != FA_OK) return st;
+    const int64_t rows = B * H * N;
+    const uint64_t pbytes = static_cast<uint64_t>(n_parts * rows * d) * 4u;
+    const uint64_t plbytes = static_cast<uint64_t>(n_parts * rows) * 4u;
+    const uint64_t tbytes = static_cast<uint64_t>(rows * d) * 2u, lbytes = static_cast<uint64_t>(rows) * 4u;
+    if (overlaps(o, tbytes, lse, lbytes)) return FA_ERR_INVALID_ARG;
+    for (const void *out : {static_cast<const void *>(o), static_cast<const void *>(lse)}) {
+        const uint64_t ob = out == o ? tbytes : lbytes;
+        if (overlaps(out, ob, o_parts, pbytes) || overlaps(out, ob, lse_parts, plbytes)) return FA_ERR_INVALID_ARG;
+    }
+    if (fa_launch_combine(o_parts, lse_parts, static_cast<int>(n_parts), rows, static_cast<int>(d), o, lse, sm_count,
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return FA_ERR_LAUNCH;
+    return FA_OK;
 }
 
 extern "C" int fa_get_device_status(void *stream)

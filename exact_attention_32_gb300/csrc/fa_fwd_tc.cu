@@ -99,13 +99,15 @@ struct Bars {
 
 __device__ __forceinline__ void report_timeout() { atomicExch(&g_tc_status, FA_ERR_TIMEOUT); }
 
-// Work unit u: 256 consecutive query rows of one (b, h) slice.  Causal units
-// are ordered heaviest row block first.  CTA c of a persistent grid of G CTAs
-// takes, in round r, unit r*G + c when r is even and r*G + (G-1-c) when r is
-// odd: the zigzag pairs heavy units with light ones, so every CTA ends up with
+// Work item u: 256 consecutive query rows of one (b, h) slice against one key
+// split (keys [split * kv_chunk, (split + 1) * kv_chunk), a multiple of 128;
+// a single split covers all keys).  Items are ordered by row block, heaviest
+// causal block first, then by split.  CTA c of a persistent grid of G CTAs
+// takes, in round r, item r*G + c when r is even and r*G + (G-1-c) when r is
+// odd: the zigzag pairs heavy items with light ones, so every CTA ends up with
 // about the same number of K/V tiles without a shared counter.
 struct Unit {
-    int bh, q_row0, n_kv;
+    int bh, q_row0, split, kv_begin, kv_end, j0, n_kv;
 };
 
 __device__ __forceinline__ int unit_index(int r)
@@ -115,22 +117,30 @@ __device__ __forceinline__ int unit_index(int r)
 }
 
 template <bool CAUSAL>
-__device__ __forceinline__ Unit unit_of(int u, int N, int BH, int n_mblocks)
+__device__ __forceinline__ Unit unit_of(int u, int N, int BH, int n_mblocks, int n_splits, int kv_chunk)
 {
-    const int mb = CAUSAL ? (n_mblocks - 1 - u / BH) : (u / BH);
+    const int rb = u / n_splits;  // row-block unit
     Unit w;
-    w.bh = u % BH;
+    w.split = u - rb * n_splits;
+    const int mb = CAUSAL ? (n_mblocks - 1 - rb / BH) : (rb / BH);
+    w.bh = rb % BH;
     w.q_row0 = mb * (kQTiles * kBlockM);
-    const int kv_end = CAUSAL ? min(N, w.q_row0 + kQTiles * kBlockM) : N;
-    w.n_kv = (kv_end + kBlockN - 1) / kBlockN;
+    w.kv_begin = w.split * kv_chunk;
+    w.kv_end = min(N, w.kv_begin + kv_chunk);
+    // keys any row of this block admits end before k_hi
+    const int k_hi = CAUSAL ? min(w.kv_end, w.q_row0 + kQTiles * kBlockM) : w.kv_end;
+    w.j0 = w.kv_begin / kBlockN;
+    w.n_kv = k_hi > w.kv_begin ? (k_hi + kBlockN - 1) / kBlockN - w.j0 : 0;
     return w;
 }
 
-template <int D, bool CAUSAL>
+// OUT_F32: O is written as fp32 (the partial results of a key split) instead
+// of bf16; split s writes its rows at o + s * B*H*N*d and lse + s * B*H*N.
+template <int D, bool CAUSAL, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ o, float *__restrict__ lse,
-                 int N, int BH, int n_mblocks, int n_units, float scale, float scale_log2)
+                 const __grid_constant__ CUtensorMap tm_v, void *__restrict__ o, float *__restrict__ lse, int N,
+                 int BH, int n_mblocks, int n_units, int n_splits, int kv_chunk, float scale, float scale_log2)
 {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -180,8 +190,9 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             prefetch_tmap(&tm_v);
             bool ok = true;
             int it = 0, uc = 0;
-            for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r), ++uc) {
-                const Unit w = unit_of<CAUSAL>(u, N, BH, n_mblocks);
+            for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
+                const Unit w = unit_of<CAUSAL>(u, N, BH, n_mblocks, n_splits, kv_chunk);
+                if (w.n_kv == 0) continue;  // no admitted key: nothing to load
                 // the Q buffers are free once the previous unit's last S MMAs have completed
                 if (!mbar_wait(bars.q_empty(), (uc & 1) ^ 1, kWaitLimitNs)) {
                     ok = false;
@@ -192,6 +203,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     for (int a = 0; a < C::kAtoms; ++a)
                         tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &tm_q, bars.q_full(), a * 64,
                                     w.q_row0 + t * kBlockM, w.bh);
+                ++uc;
                 for (int j = 0; j < w.n_kv && ok; ++j) {
                     for (int kind = 0; kind < 2; ++kind, ++it) {
                         const int slot = it % C::kStages, use = it / C::kStages;
@@ -203,10 +215,10 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         const CUtensorMap *tm = kind == 0 ? &tm_k : &tm_v;
                         for (int a = 0; a < C::kAtoms; ++a)
                             tma_load_3d(sRing + slot * C::kTileBytes + a * 16384, tm, bars.full(slot), a * 64,
-                                        j * kBlockN, w.bh);
+                                        (w.j0 + j) * kBlockN, w.bh);
                     }
                 }
-            }  // a ring wait that fails ends the body normally, so ++uc still counts its Q load
+            }
             if (!ok) report_timeout();
             // every copy this thread issued has landed before the CTA may exit
             const uint64_t lim = ok ? kWaitLimitNs : kCleanupLimitNs;
@@ -230,8 +242,9 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             constexpr uint32_t kTile16 = C::kTileBytes >> 4;
             bool ok = true;
             int it = 0, uc = 0, jg = 0;  // ring position, units done, K/V tiles done (all units)
-            for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r), ++uc) {
-                const Unit w = unit_of<CAUSAL>(u, N, BH, n_mblocks);
+            for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
+                const Unit w = unit_of<CAUSAL>(u, N, BH, n_mblocks, n_splits, kv_chunk);
+                if (w.n_kv == 0) continue;
                 if (!(ok = mbar_wait(bars.q_full(), uc & 1, kWaitLimitNs))) break;
                 tc_fence_after();
                 uint32_t prev_v_lo = 0;
@@ -282,6 +295,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     mma_commit(bars.o_full(t));
                 }
                 if (ok) mma_commit(bars.empty(prev_v));
+                ++uc;
             }
             if (!ok) report_timeout();
             // no MMA of this CTA may still be running when tensor memory is freed
@@ -297,9 +311,26 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const uint32_t tO = tmem + lane_off + 256 + t * 128;
         bool ok = true;
         int jg = 0, uc = 0;
-        for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r), ++uc) {
-            const Unit w = unit_of<CAUSAL>(u, N, BH, n_mblocks);
+        for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
+            const Unit w = unit_of<CAUSAL>(u, N, BH, n_mblocks, n_splits, kv_chunk);
             const int row_g = w.q_row0 + t * kBlockM + row;
+            const int64_t out_row = (static_cast<int64_t>(w.split) * BH + w.bh) * N + row_g;
+            if (w.n_kv == 0) {
+                // no admitted key in this split: O = 0, LSE = -inf (no weight when merged)
+                if (row_g < N) {
+                    if (OUT_F32) {
+                        float4 *orow = reinterpret_cast<float4 *>(static_cast<float *>(o) + out_row * D);
+#pragma unroll
+                        for (int i = 0; i < D / 4; ++i) orow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    } else {
+                        uint4 *orow = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(o) + out_row * D);
+#pragma unroll
+                        for (int i = 0; i < D / 8; ++i) orow[i] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    lse[out_row] = -INFINITY;
+                }
+                continue;
+            }
             float m_ref = -INFINITY;  // reference max, unscaled units
             float l = 0.f;            // exp-sum relative to m_ref (fp32 terms; gives LSE)
             float lr = 0.f;           // the same sum over the bf16-rounded terms the MMA sees (normalises O)
@@ -320,14 +351,15 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                         for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
                 }
-                const int k0 = j * kBlockN;
-                const bool need_mask =
-                    (k0 + kBlockN > N) || (CAUSAL && k0 + kBlockN - 1 > w.q_row0 + t * kBlockM);
+                const int k0 = (w.j0 + j) * kBlockN;
+                const bool need_mask = k0 < w.kv_begin || k0 + kBlockN > w.kv_end ||
+                                       (CAUSAL && k0 + kBlockN - 1 > w.q_row0 + t * kBlockM);
                 if (need_mask) {
-                    const int lim = CAUSAL ? min(N - 1, row_g) : N - 1;  // last admitted key
+                    // admitted keys: kv_begin <= key <= lim
+                    const int lim = CAUSAL ? min(w.kv_end - 1, row_g) : w.kv_end - 1;
 #pragma unroll
                     for (int i = 0; i < kBlockN; ++i)
-                        if (k0 + i > lim) s[i] = -INFINITY;
+                        if (k0 + i < w.kv_begin || k0 + i > lim) s[i] = -INFINITY;
                 }
                 // row max: eight independent chains of 3-input maxes
                 float mx[8];
@@ -403,26 +435,36 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // row dominated by one key returns that key's value without a P-rounding
             // error.  The next unit's first P V (which overwrites O_t) is issued
             // only after this warpgroup's next p_full arrive, so the reads here are safe.
-            const float inv_l = 1.f / lr;
-            __nv_bfloat16 *orow = o + (static_cast<int64_t>(w.bh) * N + row_g) * D;
+            // a row with no admitted key in this split has l = 0: O = 0, LSE = -inf
+            const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld32(tO + c * 32, r);
                 tmem_wait_ld();
                 if (row_g < N) {
+                    if (OUT_F32) {
+                        float4 *orow = reinterpret_cast<float4 *>(static_cast<float *>(o) + out_row * D + c * 32);
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(r[q4 * 8 + 0]) * inv_l, __uint_as_float(r[q4 * 8 + 1]) * inv_l);
-                        v.y = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2]) * inv_l, __uint_as_float(r[q4 * 8 + 3]) * inv_l);
-                        v.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * inv_l, __uint_as_float(r[q4 * 8 + 5]) * inv_l);
-                        v.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * inv_l, __uint_as_float(r[q4 * 8 + 7]) * inv_l);
-                        *reinterpret_cast<uint4 *>(orow + c * 32 + q4 * 8) = v;
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            orow[q4] = make_float4(__uint_as_float(r[q4 * 4 + 0]) * inv_l, __uint_as_float(r[q4 * 4 + 1]) * inv_l,
+                                                   __uint_as_float(r[q4 * 4 + 2]) * inv_l, __uint_as_float(r[q4 * 4 + 3]) * inv_l);
+                    } else {
+                        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(o) + out_row * D + c * 32;
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint4 v;
+                            v.x = pack_bf16x2(__uint_as_float(r[q4 * 8 + 0]) * inv_l, __uint_as_float(r[q4 * 8 + 1]) * inv_l);
+                            v.y = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2]) * inv_l, __uint_as_float(r[q4 * 8 + 3]) * inv_l);
+                            v.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * inv_l, __uint_as_float(r[q4 * 8 + 5]) * inv_l);
+                            v.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * inv_l, __uint_as_float(r[q4 * 8 + 7]) * inv_l);
+                            *reinterpret_cast<uint4 *>(orow + q4 * 8) = v;
+                        }
                     }
                 }
             }
-            if (row_g < N) lse[static_cast<int64_t>(w.bh) * N + row_g] = m_ref * scale + logf(l);
+            if (row_g < N) lse[out_row] = l > 0.f ? m_ref * scale + logf(l) : -INFINITY;
+            ++uc;
         }
         if (!ok) report_timeout();
     }
@@ -471,34 +513,49 @@ bool make_map(CUtensorMap *m, const void *base, int64_t BH, int64_t N, int d)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool CAUSAL>
-cudaError_t launch(const FaProblem &p, cudaStream_t stream)
+template <int D, bool CAUSAL, bool OUT_F32>
+cudaError_t launch(const FaProblem &p, void *o, float *lse, int n_splits, int kv_chunk, cudaStream_t stream)
 {
     using C = Cfg<D>;
     CUtensorMap mq, mk, mv;
     const int64_t BH = p.B * p.H;
     if (!make_map(&mq, p.q, BH, p.N, D) || !make_map(&mk, p.k, BH, p.N, D) || !make_map(&mv, p.v, BH, p.N, D))
         return cudaErrorInvalidValue;
-    auto kern = fa_fwd_tc_kernel<D, CAUSAL>;
+    auto kern = fa_fwd_tc_kernel<D, CAUSAL, OUT_F32>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t n_mblocks = (p.N + kQTiles * kBlockM - 1) / (kQTiles * kBlockM);
-    const int64_t n_units = n_mblocks * BH;
+    const int64_t n_units = n_mblocks * BH * n_splits;
     if (n_units > 0x7fffffffLL || BH > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int64_t grid = n_units < p.sm_count ? n_units : p.sm_count;  // persistent: one CTA per SM
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
     kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
-        mq, mk, mv, static_cast<__nv_bfloat16 *>(p.o), p.lse, static_cast<int>(p.N), static_cast<int>(BH),
-        static_cast<int>(n_mblocks), static_cast<int>(n_units), p.scale, scale_log2);
+        mq, mk, mv, o, lse, static_cast<int>(p.N), static_cast<int>(BH), static_cast<int>(n_mblocks),
+        static_cast<int>(n_units), n_splits, kv_chunk, p.scale, scale_log2);
     return cudaGetLastError();
+}
+
+template <bool OUT_F32>
+cudaError_t dispatch(const FaProblem &p, void *o, float *lse, int n_splits, int kv_chunk, cudaStream_t s)
+{
+    if (p.d == 64)
+        return p.causal ? launch<64, true, OUT_F32>(p, o, lse, n_splits, kv_chunk, s)
+                        : launch<64, false, OUT_F32>(p, o, lse, n_splits, kv_chunk, s);
+    return p.causal ? launch<128, true, OUT_F32>(p, o, lse, n_splits, kv_chunk, s)
+                    : launch<128, false, OUT_F32>(p, o, lse, n_splits, kv_chunk, s);
 }
 
 }  // namespace
 
 cudaError_t fa_launch_tc(const FaProblem &p, cudaStream_t stream)
 {
-    if (p.d == 64) return p.causal ? launch<64, true>(p, stream) : launch<64, false>(p, stream);
-    return p.causal ? launch<128, true>(p, stream) : launch<128, false>(p, stream);
+    return dispatch<false>(p, p.o, p.lse, 1, static_cast<int>(p.N), stream);
+}
+
+cudaError_t fa_launch_tc_partials(const FaProblem &p, float *o_parts, float *lse_parts, int n_splits, int kv_chunk,
+                                  cudaStream_t stream)
+{
+    return dispatch<true>(p, o_parts, lse_parts, n_splits, kv_chunk, stream);
 }
 
 int fa_tc_take_status(cudaStream_t stream)

@@ -18,6 +18,13 @@ struct FaProblem {
 
 // tcgen05 kernel (TMA, tensor memory, warp-specialised): 256 query rows per CTA.
 cudaError_t fa_launch_tc(const FaProblem &p, cudaStream_t stream);
+// The same kernel over n_splits key ranges of kv_chunk keys (a multiple of
+// 128): split s writes fp32 O to o_parts + s*B*H*N*d and LSE to lse_parts + s*B*H*N.
+cudaError_t fa_launch_tc_partials(const FaProblem &p, float *o_parts, float *lse_parts, int n_splits, int kv_chunk,
+                                  cudaStream_t stream);
+// Merge of n_parts partial (O fp32, LSE) results of `rows` rows into bf16 O and LSE.
+cudaError_t fa_launch_combine(const float *o_parts, const float *lse_parts, int n_parts, int64_t rows, int d,
+                              void *o, float *lse, int sm_count, cudaStream_t stream);
 // Read and clear the tcgen05 kernel's sticky device status (synchronises `stream`).
 int fa_tc_take_status(cudaStream_t stream);
 

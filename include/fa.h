@@ -85,6 +85,56 @@ int fa_fwd_mma(const void *q, const void *k, const void *v, void *o, float *lse,
                void *stream);
 
 /*
+ * Split-KV forward.  The keys are cut into `parts` contiguous ranges of
+ * `chunk` keys (chunk = 128 * ceil(ceil(N / n_splits) / 128), parts =
+ * ceil(N / chunk) <= n_splits); one launch computes, for every 256-row block
+ * and every range, the attention of those rows over that range alone (fp32
+ * O normalised over the range, and its LSE; a row with no admitted key in a
+ * range gets O = 0, LSE = -inf), and a second launch merges the parts with
+ * the two-block merge of "FlashAttention: IO-Aware Tiling, Online Softmax
+ * Mathematics, ...", section "Online Softmax Mathematics":
+ *     LSE = ln(sum_s e^LSE_s),   O = sum_s e^(LSE_s - LSE) O_s.
+ * The result equals fa_fwd's up to rounding; splitting raises the number of
+ * independent work items when B*H*ceil(N/256) is small.
+ *
+ *   q, k, v, o, lse, B, H, N, d, scale, causal : as for fa_fwd.
+ *   n_splits        : 1..32.
+ *   workspace       : device scratch owned by the caller, 16-byte aligned, at
+ *                     least fa_fwd_splitkv_workspace_bytes(...) bytes, not
+ *                     overlapping any other argument.  Holds the parts: fp32
+ *                     O [parts][B][H][N][d] followed by fp32 LSE [parts][B][H][N].
+ *                     Its contents on entry do not matter; on return they are
+ *                     the per-range results.
+ *   workspace_bytes : its size.
+ * Errors as fa_fwd; a workspace that is too small is FA_ERR_INVALID_ARG.
+ */
+int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                   int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
+                   int64_t n_splits, void *workspace, int64_t workspace_bytes,
+                   void *stream);
+
+/* Workspace bytes fa_fwd_splitkv needs for this problem, or -1 if the sizes
+ * or n_splits are invalid.  Pure host computation. */
+int64_t fa_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d,
+                                       int64_t n_splits);
+
+/*
+ * fa_combine - merge n_parts partial attention results of the same rows over
+ * disjoint key ranges (the exchange step a sequence-sharded attention needs),
+ * with the two-block merge above.
+ *
+ *   o_parts   : const fp32 [n_parts][B][H][N][d], each part normalised over its keys
+ *   lse_parts : const fp32 [n_parts][B][H][N], LSE_s (-inf: the part has no key)
+ *   n_parts   : 1..32
+ *   o         : bf16 out [B][H][N][d];  lse : fp32 out [B][H][N]
+ * A row with LSE = -inf in every part gets O = 0, LSE = -inf.  Pointers are
+ * device pointers on the current device, 16-byte aligned; outputs must not
+ * overlap inputs.  Errors as fa_fwd.
+ */
+int fa_combine(const float *o_parts, const float *lse_parts, int64_t n_parts, void *o,
+               float *lse, int64_t B, int64_t H, int64_t N, int64_t d, void *stream);
+
+/*
  * fa_get_device_status - synchronise `stream`, then return and clear the
  * current device's sticky in-kernel status (FA_OK, or FA_ERR_TIMEOUT when a
  * bounded wait inside a kernel gave up and the kernel returned early, leaving
