@@ -22,9 +22,9 @@ _lock = threading.Lock()
 
 FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_NO_DEVICE",
-                4: "FA_ERR_ARCH", 5: "FA_ERR_LAUNCH", 6: "FA_ERR_TIMEOUT"}
+                4: "FA_ERR_ARCH", 5: "FA_ERR_LAUNCH", 6: "FA_ERR_TIMEOUT", 7: "FA_ERR_WORKSPACE_LIMIT"}
 EXPORTED = ("fa_fwd", "fa_fwd_mma", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_combine",
-            "fa_get_device_status", "fa_status_string", "fa_version")
+            "fa_fwd_splitkv_noalloc", "fa_get_device_status", "fa_status_string", "fa_version")
 
 
 class FAError(RuntimeError):
@@ -53,6 +53,9 @@ def lib():
                                          ctypes.c_int, i64, vp, i64, vp]
             L.fa_fwd_splitkv_workspace_bytes.restype = i64
             L.fa_fwd_splitkv_workspace_bytes.argtypes = [i64, i64, i64, i64, i64]
+            L.fa_fwd_splitkv_noalloc.restype = ctypes.c_int
+            L.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
+                                                 ctypes.c_int, i64, vp]
             L.fa_combine.restype = ctypes.c_int
             L.fa_combine.argtypes = [vp, vp, i64, vp, vp, i64, i64, i64, i64, vp]
             L.fa_get_device_status.restype = ctypes.c_int
@@ -84,6 +87,13 @@ def fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, n_splits, workspa
 
 def fa_fwd_splitkv_workspace_bytes(B, H, N, d, n_splits) -> int:
     return lib().fa_fwd_splitkv_workspace_bytes(B, H, N, d, n_splits)
+
+
+def fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, N, d, scale, causal, n_splits, stream) -> int:
+    """Raw call of the split-KV forward whose scratch is the library's static
+    device array: for callers that cannot allocate device memory."""
+    return lib().fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), int(causal),
+                                        n_splits, stream)
 
 
 def fa_combine(o_parts, lse_parts, n_parts, o, lse, B, H, N, d, stream) -> int:

@@ -254,6 +254,8 @@ extern "C" const char *fa_status_string(int status)
     case FA_ERR_ARCH: return "FA_ERR_ARCH: device is not compute capability 10.3 (sm_103)";
     case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH: CUDA launch or execution error";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a bounded in-kernel wait gave up";
+    case FA_ERR_WORKSPACE_LIMIT:
+        return "FA_ERR_WORKSPACE_LIMIT: the problem needs more scratch than the static array holds";
     default: return "unknown fa_status";
     }
 }

@@ -44,8 +44,13 @@ enum fa_status {
     FA_ERR_NO_DEVICE = 3,   /* no CUDA device, or a pointer not on the current device */
     FA_ERR_ARCH = 4,        /* the current device is not compute capability 10.3 */
     FA_ERR_LAUNCH = 5,      /* the kernel launch itself failed (CUDA error) */
-    FA_ERR_TIMEOUT = 6      /* a bounded in-kernel wait gave up (see fa_get_device_status) */
+    FA_ERR_TIMEOUT = 6,     /* a bounded in-kernel wait gave up (see fa_get_device_status) */
+    FA_ERR_WORKSPACE_LIMIT = 7 /* fa_fwd_splitkv_noalloc: the problem needs more scratch
+                                  than FA_SPLITKV_NOALLOC_MAX_BYTES */
 };
+
+/* Size of the library-owned scratch array behind fa_fwd_splitkv_noalloc. */
+#define FA_SPLITKV_NOALLOC_MAX_BYTES (32LL * 1024 * 1024)
 
 /*
  * fa_fwd - fused exact attention forward.
@@ -117,6 +122,28 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *
  * or n_splits are invalid.  Pure host computation. */
 int64_t fa_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d,
                                        int64_t n_splits);
+
+/*
+ * fa_fwd_splitkv_noalloc - fa_fwd_splitkv for callers that cannot allocate
+ * device memory.  The pages have no counterpart: this entry point exists for
+ * host programs that must not allocate at call time (engines that plan all
+ * device memory at start-up, plugins that are handed only input and output
+ * tensors, latency-critical loops that cannot afford a cudaMalloc).
+ *
+ * Arguments, result and errors are those of fa_fwd_splitkv without the
+ * workspace: the parts go to a static device array of
+ * FA_SPLITKV_NOALLOC_MAX_BYTES (32 MiB) that every GPU loading the library
+ * holds until the process exits.  A problem whose
+ * fa_fwd_splitkv_workspace_bytes(...) exceeds it is refused with
+ * FA_ERR_WORKSPACE_LIMIT (nothing launched or written).  The first call on a
+ * device looks up the array's device address (make it before any stream
+ * capture).  No call allocates or frees device memory.  All calls share the
+ * array: calls whose kernels can overlap on the GPU (unordered streams) race
+ * and give undefined results.
+ */
+int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int64_t B, int64_t H, int64_t N, int64_t d, float scale,
+                           int causal, int64_t n_splits, void *stream);
 
 /*
  * fa_combine - merge n_parts partial attention results of the same rows over
