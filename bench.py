@@ -54,6 +54,8 @@ def parse_args():
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-secondary", action="store_true",
+                   help="skip the split-KV merge (fa_combine) memory-roofline measurement")
     return p.parse_args()
 
 
@@ -179,6 +181,43 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ secondary row
+
+def combine_roofline(w, dev, peaks, peak_src, n_parts=4, steps=20):
+    """fa_combine (the split-KV merge) on synthetic fp32 parts shaped like the
+    workload: a memory-bound kernel, reported against the measured copy
+    bandwidth.  Algorithmic bytes per launch: every part read once
+    (S * rows * (4d + 4)), O and LSE written once (rows * (2d + 4))."""
+    import exact_attention_32_gb300 as fa
+    rows = w.B * w.H * w.N
+    g = torch.Generator(device="cpu").manual_seed(w.seed)
+    o_parts = torch.randn((n_parts, w.B, w.H, w.N, w.d), generator=g).to(dev)
+    lse_parts = (torch.randn((n_parts, w.B, w.H, w.N), generator=g) * 4).to(dev)
+    o = torch.empty((w.B, w.H, w.N, w.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    args = (o_parts.data_ptr(), lse_parts.data_ptr(), n_parts, o.data_ptr(), lse.data_ptr(),
+            w.B, w.H, w.N, w.d, stream.cuda_stream)
+    for _ in range(3):
+        if fa.fa_combine(*args) != 0:
+            raise fa.FAError(fa.fa_combine(*args), "fa_combine")
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fa.fa_combine(*args)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = n_parts * rows * (4 * w.d + 4) + rows * (2 * w.d + 4)
+    peak = float(peaks["hbm_gbs"])
+    achieved = nbytes / (ms / 1e3) / 1e9
+    return {"kernel": "fa_combine_kernel", "row": "split-KV merge of partial (O, LSE)", "bound": "hbm",
+            "parts": n_parts, "achieved": achieved, "peak": peak, "peak_source": f"{peak_src} hbm_gbs",
+            "unit": "GB/s", "frac": achieved / peak, "algorithmic_bytes_per_launch": nbytes,
+            "launch_ms": ms, "data": "synthetic fp32 parts, inputs larger than L2"}
 
 
 # ------------------------------------------------------------- CPU baseline
@@ -348,6 +387,8 @@ def run_ours(args, rank, world, local):
     if e2e:
         line["e2e"] = e2e
     line["clocks"] = clk
+    if not args.no_secondary:
+        line["secondary"] = [combine_roofline(w, dev, peaks, peak_src)]
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     return line

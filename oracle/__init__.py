@@ -23,6 +23,13 @@ Independent references, each in fp64 or better:
 ``merge``              the two-block merge of "FlashAttention: IO-Aware Tiling,
                        ...", section "Online Softmax Mathematics", folding
                        partial (O, LSE) results over disjoint key ranges.
+``attention_backward`` gradients dQ, dK, dV of sum(O * dO), in numpy fp64, by
+                       the formulas of "6.1 FlashAttention V1 in detail",
+                       section 6.1 (dV = P^T dO, dP = dO V^T, D = rowsum(dO * O)
+                       = rowsum(dP * P), dS = P * (dP - D)) and of the
+                       llms.blog page, section "Backward Pass Recomputation"
+                       (dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d), with 1/sqrt(d)
+                       read as the scale), dense per (b, h) slice.
 ``attention_decimal``  brute force in Python ``decimal`` at 50 digits, using
                        the softmax definition directly (exp(s_j) / sum exp(s_k),
                        no max shift) - an independent formulation for tiny
@@ -236,6 +243,47 @@ def merge(o_parts, lse_parts):
     with np.errstate(divide="ignore"):
         lse = np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), -np.inf)
     return o, lse
+
+
+def attention_backward(q, k, v, do, scale: float, causal: bool, slices=None):
+    """fp64 gradients of sum(O * dO) with respect to Q, K and V.
+
+    q, k, v, do : bf16 CPU tensors [B, H, N, d] (widened exactly)
+    slices      : None (all) or an iterable of flat slice ids b*H + h
+    Per slice, dense: S = scale Q K^T (causal: -inf above the diagonal),
+    P by the three-pass safe softmax, O = P V; then dV = P^T dO,
+    dP = dO V^T, D_i = rowsum(dO * O)_i, dS = P * (dP - D),
+    dQ = scale dS K, dK = scale dS^T Q.
+    Returns dict of float64 arrays dq, dk, dv ([n_slices, N, d]), o
+    ([n_slices, N, d]), lse and D ([n_slices, N]), in the order of `slices`.
+    """
+    qd, kd, vd, dod = (_as_f64(t) for t in (q, k, v, do))
+    B, H, N, d = qd.shape
+    qd, kd, vd, dod = (x.reshape(B * H, N, d) for x in (qd, kd, vd, dod))
+    ids = list(range(B * H)) if slices is None else [int(x) for x in slices]
+    out = {name: [] for name in ("dq", "dk", "dv", "o", "lse", "D")}
+    mask = np.triu(np.ones((N, N), dtype=bool), k=1) if causal else None
+    for bh in ids:
+        Q, K, V, dO = qd[bh], kd[bh], vd[bh], dod[bh]
+        S = scale * (Q @ K.T)
+        if causal:
+            S[mask] = -np.inf
+        m = S.max(axis=1, keepdims=True)          # pass 1
+        E = np.exp(S - m)
+        l = E.sum(axis=1, keepdims=True)          # pass 2
+        P = E / l                                 # pass 3
+        O = P @ V
+        dV = P.T @ dO
+        dP = dO @ V.T
+        D = (dO * O).sum(axis=1, keepdims=True)
+        dS = P * (dP - D)
+        out["dq"].append(scale * (dS @ K))
+        out["dk"].append(scale * (dS.T @ Q))
+        out["dv"].append(dV)
+        out["o"].append(O)
+        out["lse"].append((m + np.log(l))[:, 0])
+        out["D"].append(D[:, 0])
+    return {name: np.stack(vals) for name, vals in out.items()}
 
 
 def attention_decimal(q, k, v, scale, causal: bool, digits: int = 50):
