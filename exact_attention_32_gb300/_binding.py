@@ -24,7 +24,8 @@ FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_NO_DEVICE",
                 4: "FA_ERR_ARCH", 5: "FA_ERR_LAUNCH", 6: "FA_ERR_TIMEOUT", 7: "FA_ERR_WORKSPACE_LIMIT"}
 EXPORTED = ("fa_fwd", "fa_fwd_mma", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_combine",
-            "fa_fwd_splitkv_noalloc", "fa_get_device_status", "fa_status_string", "fa_version")
+            "fa_fwd_splitkv_noalloc", "fa_bwd", "fa_bwd_workspace_bytes", "fa_get_device_status",
+            "fa_status_string", "fa_version")
 
 
 class FAError(RuntimeError):
@@ -56,6 +57,10 @@ def lib():
             L.fa_fwd_splitkv_noalloc.restype = ctypes.c_int
             L.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
                                                  ctypes.c_int, i64, vp]
+            L.fa_bwd.restype = ctypes.c_int
+            L.fa_bwd.argtypes = [vp] * 9 + [i64, i64, i64, i64, ctypes.c_float, ctypes.c_int, vp, i64, vp]
+            L.fa_bwd_workspace_bytes.restype = i64
+            L.fa_bwd_workspace_bytes.argtypes = [i64] * 4
             L.fa_combine.restype = ctypes.c_int
             L.fa_combine.argtypes = [vp, vp, i64, vp, vp, i64, i64, i64, i64, vp]
             L.fa_get_device_status.restype = ctypes.c_int
@@ -94,6 +99,17 @@ def fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, N, d, scale, causal, n_splits,
     device array: for callers that cannot allocate device memory."""
     return lib().fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), int(causal),
                                         n_splits, stream)
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes,
+           stream) -> int:
+    """Raw call of the backward (caller-owned workspace)."""
+    return lib().fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, ctypes.c_float(scale), int(causal),
+                        workspace, workspace_bytes, stream)
+
+
+def fa_bwd_workspace_bytes(B, H, N, d) -> int:
+    return lib().fa_bwd_workspace_bytes(B, H, N, d)
 
 
 def fa_combine(o_parts, lse_parts, n_parts, o, lse, B, H, N, d, stream) -> int:
@@ -203,3 +219,31 @@ def combine(o_parts: torch.Tensor, lse_parts: torch.Tensor, stream: torch.cuda.S
     if st != FA_OK:
         raise FAError(st, "fa_combine")
     return o, lse
+
+
+def backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+             dout: torch.Tensor, scale: float | None = None, causal: bool = False,
+             workspace: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None):
+    """(dQ, dK, dV) by ``fa_bwd``; o and lse are ``forward``'s outputs.  The
+    workspace (uint8 CUDA tensor) is allocated with torch when not given."""
+    for t in (q, k, v, o, dout):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.shape != q.shape:
+            raise ValueError("q, k, v, o, dout must be contiguous bf16 CUDA tensors of one shape")
+    B, H, N, d = q.shape
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B, H, N]")
+    scale = default_scale(d) if scale is None else scale
+    need = fa_bwd_workspace_bytes(B, H, N, d)
+    if need < 0:
+        raise FAError(1 if d in (64, 128) else 2, "fa_bwd_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                    dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, float(scale), bool(causal),
+                    workspace.data_ptr(), workspace.numel() * workspace.element_size(), s.cuda_stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_bwd")
+    return dq, dk, dv

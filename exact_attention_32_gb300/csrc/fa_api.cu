@@ -235,13 +235,68 @@ extern "C" int fa_combine(const float *o_parts, const float *lse_parts, int64_t 
     return FA_OK;
 }
 
+extern "C" int64_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d)
+{
+    if (check_sizes(B, H, N, d) != FA_OK) return -1;
+    return fa_bwd_workspace_size(B, H, N, d);
+}
+
+extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                      const void *dout, void *dq, void *dk, void *dv, int64_t B, int64_t H, int64_t N, int64_t d,
+                      float scale, int causal, void *workspace, int64_t workspace_bytes, void *stream)
+{
+    int st = check_sizes(B, H, N, d);
+    if (st != FA_OK) return st;
+    if ((causal != 0 && causal != 1) || !(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+    const int64_t need = fa_bwd_workspace_size(B, H, N, d);
+    if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
+    int dev = 0, sm_count = 0;
+    if ((st = current_device(&dev, &sm_count)) != FA_OK) return st;
+    const void *ptrs[11] = {q, k, v, o, lse, dout, dq, dk, dv, workspace, nullptr};
+    for (int i = 0; i < 10; ++i)
+        if ((st = check_pointer(ptrs[i], dev)) != FA_OK) return st;
+    const uint64_t tbytes = static_cast<uint64_t>(B * H * N * d) * 2u;
+    const uint64_t lbytes = static_cast<uint64_t>(B * H * N) * 4u;
+    const void *outs[4] = {dq, dk, dv, workspace};
+    const uint64_t osz[4] = {tbytes, tbytes, tbytes, static_cast<uint64_t>(need)};
+    const void *ins[6] = {q, k, v, o, lse, dout};
+    const uint64_t isz[6] = {tbytes, tbytes, tbytes, tbytes, lbytes, tbytes};
+    for (int a = 0; a < 4; ++a) {
+        for (int b = 0; b < 6; ++b)
+            if (overlaps(outs[a], osz[a], ins[b], isz[b])) return FA_ERR_INVALID_ARG;
+        for (int b = a + 1; b < 4; ++b)
+            if (overlaps(outs[a], osz[a], outs[b], osz[b])) return FA_ERR_INVALID_ARG;
+    }
+    FaBwdProblem p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.lse = lse;
+    p.dout = dout;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.d = static_cast<int>(d);
+    p.scale = scale;
+    p.causal = causal;
+    p.sm_count = sm_count;
+    if (fa_launch_bwd(p, workspace, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_LAUNCH;
+    return FA_OK;
+}
+
 extern "C" int fa_get_device_status(void *stream)
 {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return FA_ERR_LAUNCH;
     }
-    return fa_tc_take_status(static_cast<cudaStream_t>(stream));
+    const int fwd = fa_tc_take_status(static_cast<cudaStream_t>(stream));
+    const int bwd = fa_bwd_take_status(static_cast<cudaStream_t>(stream));
+    return fwd != FA_OK ? fwd : bwd;
 }
 
 extern "C" const char *fa_status_string(int status)

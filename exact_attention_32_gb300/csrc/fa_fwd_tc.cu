@@ -335,7 +335,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             float l = 0.f;            // exp-sum relative to m_ref (fp32 terms; gives LSE)
             float lr = 0.f;           // the same sum over the bf16-rounded terms the MMA sees (normalises O)
             for (int j = 0; j < w.n_kv; ++j, ++jg) {
-                if (!mbar_wait(bars.s_full(t), jg & 1, kWaitLimitNs)) {
+                if (!mbar_wait_warp(bars.s_full(t), jg & 1, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
@@ -427,7 +427,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bars.p_full(t));
             }
-            if (!ok || !(ok = mbar_wait(bars.o_full(t), uc & 1, kWaitLimitNs))) break;
+            if (!ok || !(ok = mbar_wait_warp(bars.o_full(t), uc & 1, kWaitLimitNs))) break;
             tc_fence_after();
             // epilogue: O = u / l in bf16 straight from registers to global memory.
             // u was accumulated from bf16-rounded P, so it is divided by the sum of

@@ -28,5 +28,23 @@ cudaError_t fa_launch_combine(const float *o_parts, const float *lse_parts, int 
 // Read and clear the tcgen05 kernel's sticky device status (synchronises `stream`).
 int fa_tc_take_status(cudaStream_t stream);
 
+// One validated backward problem: gradients of sum(O * dO).
+struct FaBwdProblem {
+    const void *q, *k, *v, *o, *dout;
+    const float *lse;
+    void *dq, *dk, *dv;
+    int64_t B, H, N;
+    int d;
+    float scale;
+    int causal;
+    int sm_count;
+};
+// Workspace bytes of the backward: fp32 dQ accumulator and two padded fp32 row vectors.
+int64_t fa_bwd_workspace_size(int64_t B, int64_t H, int64_t N, int64_t d);
+// Pre (D, LSE log2 e, zero accumulator) + tcgen05 main kernel + post (dQ to bf16).
+cudaError_t fa_launch_bwd(const FaBwdProblem &p, void *workspace, cudaStream_t stream);
+// Read and clear the backward kernel's sticky device status (synchronises `stream`).
+int fa_bwd_take_status(cudaStream_t stream);
+
 // Warp-level tensor-core (mma.sync) kernel: one CTA per 128-row query tile.
 cudaError_t fa_launch_mma(const FaProblem &p, cudaStream_t stream);

@@ -74,6 +74,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
+// mbar_wait for a whole warp: every lane waits (bounded) and the result is the
+// same on all lanes, so warp-collective tcgen05 operations after it are never
+// issued by part of a warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit_ns));
+}
+
 // ---------------------------------------------------------------- TMA copies
 
 // 3-D tiled bulk tensor load global -> shared, completing on `bar` (tx bytes).
@@ -93,6 +101,23 @@ __device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];\n" ::"l"(
                      reinterpret_cast<uint64_t>(tmap)),
                  "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+// Plain (untiled) bulk copy global -> shared of `bytes` (multiple of 16, both
+// addresses 16-byte aligned), completing on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Four fp32 additions to 16-byte-aligned global memory in one reduction.
+__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
 }
 
@@ -148,12 +173,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 }
 
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, dense.
-// b_mn_major: B is stored with its N index contiguous (else K contiguous).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major)
+// b_mn_major: B is stored with its N index contiguous (else K contiguous);
+// a_mn_major: A is stored with its M index contiguous (else K contiguous).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major, bool a_mn_major = false)
 {
     return (1u << 4)                                 // D format: f32
            | (1u << 7)                               // A format: bf16
            | (1u << 10)                              // B format: bf16
+           | ((a_mn_major ? 1u : 0u) << 15)          // A major-ness
            | ((b_mn_major ? 1u : 0u) << 16)          // B major-ness
            | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16

@@ -85,6 +85,15 @@ def make_inputs(B: int, H: int, N: int, d: int, seed: int, q_gain: float = 1.0,
     return tuple(out)
 
 
+def make_grad_output(B: int, H: int, N: int, d: int, seed: int, device="cpu"):
+    """A seeded upstream gradient dO for the backward: iid N(0,1) fp32 from a
+    CPU generator seeded with ``seed + 7919``, rounded to bf16."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed) + 7919)
+    t = torch.randn((B, H, N, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return t.to(device) if str(device) != "cpu" else t
+
+
 def workload_inputs(w: Workload, device="cpu", seed=None):
     """Inputs of a named workload (its own seed unless one is given)."""
     return make_inputs(w.B, w.H, w.N, w.d, w.seed if seed is None else seed,

@@ -162,6 +162,35 @@ int fa_combine(const float *o_parts, const float *lse_parts, int64_t n_parts, vo
                float *lse, int64_t B, int64_t H, int64_t N, int64_t d, void *stream);
 
 /*
+ * fa_bwd - gradients of sum(O * dO) with respect to Q, K and V for the
+ * attention fa_fwd computes ("6.1 FlashAttention V1 in detail", section 6:
+ * dV = P^T dO, dP = dO V^T, D = rowsum(dO * O), dS = P * (dP - D); and
+ * "FlashAttention: IO-Aware Tiling, ...", section "Backward Pass
+ * Recomputation": dQ = scale * dS K, dK = scale * dS^T Q).  P is recomputed
+ * from the saved LSE, never stored.
+ *
+ *   q, k, v     : const bf16 [B, H, N, d], as passed to fa_fwd
+ *   o, lse      : const, fa_fwd's outputs for q, k, v, scale, causal
+ *   dout        : const bf16 [B, H, N, d], the gradient of the loss w.r.t. O
+ *   dq, dk, dv  : bf16 out [B, H, N, d]
+ *   B, H, N, d, scale, causal : as for fa_fwd
+ *   workspace   : device scratch owned by the caller, 16-byte aligned, at least
+ *                 fa_bwd_workspace_bytes(B, H, N, d) bytes (an fp32 dQ
+ *                 accumulator and two fp32 row vectors); contents on entry do
+ *                 not matter
+ * Outputs and workspace must not overlap the inputs or each other.  Three
+ * launches on `stream`; errors as fa_fwd.
+ */
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+           const void *dout, void *dq, void *dk, void *dv, int64_t B, int64_t H, int64_t N,
+           int64_t d, float scale, int causal, void *workspace, int64_t workspace_bytes,
+           void *stream);
+
+/* Workspace bytes fa_bwd needs (B*H*N*d*4 + 2*B*H*ceil(N/128)*128*4), or -1
+ * for invalid sizes.  Pure host computation. */
+int64_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d);
+
+/*
  * fa_get_device_status - synchronise `stream`, then return and clear the
  * current device's sticky in-kernel status (FA_OK, or FA_ERR_TIMEOUT when a
  * bounded wait inside a kernel gave up and the kernel returned early, leaving
