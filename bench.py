@@ -55,7 +55,7 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-secondary", action="store_true",
-                   help="skip the split-KV merge (fa_combine) memory-roofline measurement")
+                   help="skip the secondary rows: split-KV merge roofline and backward throughput")
     return p.parse_args()
 
 
@@ -218,6 +218,42 @@ def combine_roofline(w, dev, peaks, peak_src, n_parts=4, steps=20):
             "parts": n_parts, "achieved": achieved, "peak": peak, "peak_source": f"{peak_src} hbm_gbs",
             "unit": "GB/s", "frac": achieved / peak, "algorithmic_bytes_per_launch": nbytes,
             "launch_ms": ms, "data": "synthetic fp32 parts, inputs larger than L2"}
+
+
+def backward_throughput(w, dev, peaks, peak_src, steps=10):
+    """fa_bwd (pre + tcgen05 main + post launches) on the workload with a seeded
+    dO: conventional backward FLOPs 2.5 x the forward's (five N^2 d products
+    instead of two), halved when causal."""
+    import exact_attention_32_gb300 as fa
+    from exact_attention_32_gb300.workloads import make_grad_output
+    q, k, v = (t.to(dev) for t in workload_inputs(w))
+    do = make_grad_output(w.B, w.H, w.N, w.d, w.seed, device=dev)
+    o, lse = fa.forward(q, k, v, scale=w.scale, causal=w.causal)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    stream = torch.cuda.current_stream(dev)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H, w.N, w.d, w.scale, w.causal,
+            ws.data_ptr(), ws.numel(), stream.cuda_stream)
+    for _ in range(3):
+        st = fa.fa_bwd(*args)
+        if st != 0:
+            raise fa.FAError(st, "fa_bwd")
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fa.fa_bwd(*args)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    flops = 2.5 * w.flops
+    peak = float(peaks["bf16_tflops"])
+    achieved = flops / (ms / 1e3) / 1e12
+    return {"kernel": "fa_bwd_tc_kernel (+ pre, post)", "row": "backward dQ, dK, dV", "bound": "tensor",
+            "achieved": achieved, "peak": peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
+            "unit": "TFLOP/s", "frac": achieved / peak, "algorithmic_flops_per_step": flops,
+            "ms_per_step": ms, "launches_per_step": 3}
 
 
 # ------------------------------------------------------------- CPU baseline
@@ -388,7 +424,8 @@ def run_ours(args, rank, world, local):
         line["e2e"] = e2e
     line["clocks"] = clk
     if not args.no_secondary:
-        line["secondary"] = [combine_roofline(w, dev, peaks, peak_src)]
+        line["secondary"] = [combine_roofline(w, dev, peaks, peak_src),
+                             backward_throughput(w, dev, peaks, peak_src)]
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     return line
