@@ -55,7 +55,7 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-secondary", action="store_true",
-                   help="skip the secondary rows: split-KV merge roofline and backward throughput")
+                   help="skip the secondary rows: split-KV merge, backward and FP8 forward")
     return p.parse_args()
 
 
@@ -256,6 +256,41 @@ def backward_throughput(w, dev, peaks, peak_src, steps=10):
             "ms_per_step": ms, "launches_per_step": 3}
 
 
+def fp8_throughput(w, dev, peaks, peak_src, steps=20):
+    """fa_fwd_fp8 on the workload encoded as E4M3 per (b, h) (power-of-two
+    scales).  Peak: the measured bf16 peak times the nominal dense E4M3/bf16
+    ratio of 2 (4.5 vs 2.25 PFLOP/s)."""
+    import exact_attention_32_gb300 as fa
+    from exact_attention_32_gb300.workloads import quantize_e4m3
+    if w.d != 128:
+        return None
+    enc = [quantize_e4m3(t) for t in workload_inputs(w)]
+    (q8, qs, _), (k8, ks, _), (v8, vs, _) = [(a.to(dev), b.to(dev), None) for a, b, _ in enc]
+    o = torch.empty((w.B, w.H, w.N, w.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    args = (q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), qs.data_ptr(), ks.data_ptr(), vs.data_ptr(),
+            o.data_ptr(), lse.data_ptr(), w.B, w.H, w.N, w.d, w.scale, w.causal, stream.cuda_stream)
+    for _ in range(3):
+        st = fa.fa_fwd_fp8(*args)
+        if st != 0:
+            raise fa.FAError(st, "fa_fwd_fp8")
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fa.fa_fwd_fp8(*args)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    peak = 2.0 * float(peaks["bf16_tflops"])
+    achieved = w.flops / (ms / 1e3) / 1e12
+    return {"kernel": "fa_fwd_tc_kernel (E4M3)", "row": "FP8 forward", "bound": "tensor", "achieved": achieved,
+            "peak": peak, "peak_source": f"{peak_src} bf16_tflops x 2 (nominal E4M3/bf16 dense ratio)",
+            "unit": "TFLOP/s", "frac": achieved / peak, "algorithmic_flops_per_launch": w.flops,
+            "launch_ms": ms}
+
+
 # ------------------------------------------------------------- CPU baseline
 
 def oracle_rows_for(w, seconds: float, threads: int, rng_seed: int = 0):
@@ -424,8 +459,9 @@ def run_ours(args, rank, world, local):
         line["e2e"] = e2e
     line["clocks"] = clk
     if not args.no_secondary:
-        line["secondary"] = [combine_roofline(w, dev, peaks, peak_src),
-                             backward_throughput(w, dev, peaks, peak_src)]
+        sec = [combine_roofline(w, dev, peaks, peak_src), backward_throughput(w, dev, peaks, peak_src),
+               fp8_throughput(w, dev, peaks, peak_src)]
+        line["secondary"] = [x for x in sec if x is not None]
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     return line

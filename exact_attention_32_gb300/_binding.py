@@ -24,7 +24,7 @@ FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_NO_DEVICE",
                 4: "FA_ERR_ARCH", 5: "FA_ERR_LAUNCH", 6: "FA_ERR_TIMEOUT", 7: "FA_ERR_WORKSPACE_LIMIT"}
 EXPORTED = ("fa_fwd", "fa_fwd_mma", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_combine",
-            "fa_fwd_splitkv_noalloc", "fa_bwd", "fa_bwd_workspace_bytes", "fa_get_device_status",
+            "fa_fwd_splitkv_noalloc", "fa_fwd_fp8", "fa_bwd", "fa_bwd_workspace_bytes", "fa_get_device_status",
             "fa_status_string", "fa_version")
 
 
@@ -57,6 +57,8 @@ def lib():
             L.fa_fwd_splitkv_noalloc.restype = ctypes.c_int
             L.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
                                                  ctypes.c_int, i64, vp]
+            L.fa_fwd_fp8.restype = ctypes.c_int
+            L.fa_fwd_fp8.argtypes = [vp] * 8 + [i64, i64, i64, i64, ctypes.c_float, ctypes.c_int, vp]
             L.fa_bwd.restype = ctypes.c_int
             L.fa_bwd.argtypes = [vp] * 9 + [i64, i64, i64, i64, ctypes.c_float, ctypes.c_int, vp, i64, vp]
             L.fa_bwd_workspace_bytes.restype = i64
@@ -99,6 +101,11 @@ def fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, N, d, scale, causal, n_splits,
     device array: for callers that cannot allocate device memory."""
     return lib().fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), int(causal),
                                         n_splits, stream)
+
+
+def fa_fwd_fp8(q, k, v, qs, ks, vs, o, lse, B, H, N, d, scale, causal, stream) -> int:
+    """Raw call of the E4M3 forward (per-(b, h) fp32 scales)."""
+    return lib().fa_fwd_fp8(q, k, v, qs, ks, vs, o, lse, B, H, N, d, ctypes.c_float(scale), int(causal), stream)
 
 
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes,
@@ -247,3 +254,28 @@ def backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     if st != FA_OK:
         raise FAError(st, "fa_bwd")
     return dq, dk, dv
+
+
+def forward_fp8(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale: torch.Tensor,
+                k_scale: torch.Tensor, v_scale: torch.Tensor, scale: float | None = None,
+                causal: bool = False, stream: torch.cuda.Stream | None = None):
+    """(O bf16, LSE fp32) by ``fa_fwd_fp8``: q8, k8, v8 are float8_e4m3fn (or
+    uint8) CUDA tensors [B, H, N, 128]; the scales fp32 [B, H] (or [B*H])."""
+    for t in (q8, k8, v8):
+        if t.element_size() != 1 or not t.is_cuda or not t.is_contiguous() or t.shape != q8.shape:
+            raise ValueError("q8, k8, v8 must be contiguous 8-bit CUDA tensors of one shape")
+    B, H, N, d = q8.shape
+    for t in (q_scale, k_scale, v_scale):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or t.numel() != B * H:
+            raise ValueError("scales must be contiguous fp32 CUDA tensors with B*H elements")
+    scale = default_scale(d) if scale is None else scale
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q8.device)
+    with torch.cuda.device(q8.device):
+        st = fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), q_scale.data_ptr(), k_scale.data_ptr(),
+                        v_scale.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, float(scale),
+                        bool(causal), s.cuda_stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_fp8")
+    return o, lse

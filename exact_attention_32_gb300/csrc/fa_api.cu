@@ -235,6 +235,45 @@ extern "C" int fa_combine(const float *o_parts, const float *lse_parts, int64_t 
     return FA_OK;
 }
 
+extern "C" int fa_fwd_fp8(const void *q, const void *k, const void *v, const float *q_scale,
+                          const float *k_scale, const float *v_scale, void *o, float *lse, int64_t B, int64_t H,
+                          int64_t N, int64_t d, float scale, int causal, void *stream)
+{
+    int st = check_sizes(B, H, N, d);
+    if (st != FA_OK) return st;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if ((causal != 0 && causal != 1) || !(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+    int dev = 0, sm_count = 0;
+    if ((st = current_device(&dev, &sm_count)) != FA_OK) return st;
+    const void *ptrs[8] = {q, k, v, q_scale, k_scale, v_scale, o, lse};
+    for (const void *p : ptrs)
+        if ((st = check_pointer(p, dev)) != FA_OK) return st;
+    const uint64_t in_bytes = static_cast<uint64_t>(B * H * N * d);  // one byte per E4M3 element
+    const uint64_t o_bytes = in_bytes * 2u, lbytes = static_cast<uint64_t>(B * H * N) * 4u;
+    const uint64_t sbytes = static_cast<uint64_t>(B * H) * 4u;
+    if (overlaps(o, o_bytes, lse, lbytes)) return FA_ERR_INVALID_ARG;
+    const void *ins[6] = {q, k, v, q_scale, k_scale, v_scale};
+    const uint64_t isz[6] = {in_bytes, in_bytes, in_bytes, sbytes, sbytes, sbytes};
+    for (int i = 0; i < 6; ++i)
+        if (overlaps(o, o_bytes, ins[i], isz[i]) || overlaps(lse, lbytes, ins[i], isz[i])) return FA_ERR_INVALID_ARG;
+    FaProblem p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.lse = lse;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.d = static_cast<int>(d);
+    p.scale = scale;
+    p.causal = causal;
+    p.sm_count = sm_count;
+    if (fa_launch_tc_fp8(p, q_scale, k_scale, v_scale, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return FA_ERR_LAUNCH;
+    return FA_OK;
+}
+
 extern "C" int64_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d)
 {
     if (check_sizes(B, H, N, d) != FA_OK) return -1;

@@ -71,11 +71,16 @@ constexpr uint64_t kCleanupLimitNs = 20000000ull;    // 20 ms per wait while win
 
 __device__ int g_tc_status;  // sticky FA_ERR_TIMEOUT, read and cleared by fa_get_device_status
 
-template <int D>
+template <int D, bool FP8>
 struct Cfg {
-    static constexpr int kTileBytes = kBlockN * D * 2;  // one Q, K or V tile (bf16)
-    static constexpr int kAtoms = D / 64;               // 128-byte-wide column blocks per tile
-    static constexpr int kStages = D == 128 ? 4 : 8;    // K/V ring slots
+    static constexpr int kElem = FP8 ? 1 : 2;               // bytes per element (E4M3 or bf16)
+    static constexpr int kRowBytes = D * kElem;
+    static constexpr int kTileBytes = kBlockN * kRowBytes;  // one Q, K or V tile
+    static constexpr int kAtoms = kRowBytes / 128;          // 128-byte-wide column blocks per tile
+    static constexpr int kStages = kTileBytes == 32768 ? 4 : 8;  // K/V ring slots
+    static constexpr int kSSteps = kRowBytes / 32;          // S MMA K steps (32 bytes of each row)
+    static constexpr int kPVKeys = FP8 ? 32 : 16;           // keys per P V MMA
+    static constexpr int kPVSteps = kBlockN / kPVKeys;
     static constexpr int kBarOffset = (kQTiles + kStages) * kTileBytes;
     // barriers: q_full, q_empty, s_full[2], p_full[2], o_full[2], mma_done, kv_full[S], kv_empty[S]
     static constexpr int kNumBars = 9 + 2 * kStages;
@@ -136,13 +141,18 @@ __device__ __forceinline__ Unit unit_of(int u, int N, int BH, int n_mblocks, int
 
 // OUT_F32: O is written as fp32 (the partial results of a key split) instead
 // of bf16; split s writes its rows at o + s * B*H*N*d and lse + s * B*H*N.
-template <int D, bool CAUSAL, bool OUT_F32>
+// FP8: Q, K, V are E4M3 with one fp32 scale per (b, h) each (qs, ks, vs): the
+// S MMAs see the raw E4M3 values and the scales are folded into the exponent
+// constant and the LSE; P is rounded to E4M3 for a kind::f8f6f4 P V MMA and vs
+// is applied in the epilogue.
+template <int D, bool CAUSAL, bool OUT_F32, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, void *__restrict__ o, float *__restrict__ lse, int N,
-                 int BH, int n_mblocks, int n_units, int n_splits, int kv_chunk, float scale, float scale_log2)
+                 int BH, int n_mblocks, int n_units, int n_splits, int kv_chunk, float scale, float scale_log2,
+                 const float *__restrict__ qs, const float *__restrict__ ks, const float *__restrict__ vs)
 {
-    using C = Cfg<D>;
+    using C = Cfg<D, FP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s_base = smem_u32(smem);
@@ -201,7 +211,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 mbar_arrive_expect_tx(bars.q_full(), kQTiles * C::kTileBytes);
                 for (int t = 0; t < kQTiles; ++t)
                     for (int a = 0; a < C::kAtoms; ++a)
-                        tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &tm_q, bars.q_full(), a * 64,
+                        tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &tm_q, bars.q_full(), a * (128 / C::kElem),
                                     w.q_row0 + t * kBlockM, w.bh);
                 ++uc;
                 for (int j = 0; j < w.n_kv && ok; ++j) {
@@ -214,8 +224,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
                         const CUtensorMap *tm = kind == 0 ? &tm_k : &tm_v;
                         for (int a = 0; a < C::kAtoms; ++a)
-                            tma_load_3d(sRing + slot * C::kTileBytes + a * 16384, tm, bars.full(slot), a * 64,
-                                        (w.j0 + j) * kBlockN, w.bh);
+                            tma_load_3d(sRing + slot * C::kTileBytes + a * 16384, tm, bars.full(slot),
+                                        a * (128 / C::kElem), (w.j0 + j) * kBlockN, w.bh);
                     }
                 }
             }
@@ -229,8 +239,9 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------- MMA issue
         if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(kBlockM, kBlockN, false);
-            constexpr uint32_t idO = idesc_bf16_f32(kBlockM, D, true);
+            constexpr uint32_t idS = FP8 ? idesc_e4m3_f32(kBlockM, kBlockN, false)
+                                         : idesc_bf16_f32(kBlockM, kBlockN, false);
+            constexpr uint32_t idO = FP8 ? idesc_e4m3_f32(kBlockM, D, true) : idesc_bf16_f32(kBlockM, D, true);
             // descriptors are built once; a K step only moves the start address
             // (low 32 bits, in 16-byte units): +32 bytes inside a 128-byte-wide
             // column block, +16 KB to the next block (S), +2 KB per 16 keys (P V)
@@ -262,16 +273,26 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             if (!(ok = mbar_wait(bars.p_full(t), (jg - 1) & 1, kWaitLimitNs))) break;
                             tc_fence_after();
 #pragma unroll
-                            for (int kk = 0; kk < kBlockN / 16; ++kk)
-                                mma_ts_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + kk * 128,
-                                            dv_hi, idO, (j > 1 || kk > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < C::kPVSteps; ++kk) {
+                                const uint32_t boff = (kk * C::kPVKeys * 128) >> 4;
+                                if constexpr (FP8)
+                                    mma_ts_f8_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + boff,
+                                                   dv_hi, idO, (j > 1 || kk > 0) ? 1u : 0u);
+                                else
+                                    mma_ts_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + boff,
+                                                dv_hi, idO, (j > 1 || kk > 0) ? 1u : 0u);
+                            }
                         }
                         const uint32_t aq_lo = dq_lo + t * kTile16;
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
+                        for (int kk = 0; kk < C::kSSteps; ++kk) {
                             const uint32_t koff = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
-                            mma_ss_lohi(tmem + t * 128, aq_lo + koff, dq_hi, dk_lo + koff, dk_hi, idS,
-                                        kk > 0 ? 1u : 0u);
+                            if constexpr (FP8)
+                                mma_ss_f8_lohi(tmem + t * 128, aq_lo + koff, dq_hi, dk_lo + koff, dk_hi, idS,
+                                               kk > 0 ? 1u : 0u);
+                            else
+                                mma_ss_lohi(tmem + t * 128, aq_lo + koff, dq_hi, dk_lo + koff, dk_hi, idS,
+                                            kk > 0 ? 1u : 0u);
                         }
                         mma_commit(bars.s_full(t));
                     }
@@ -289,9 +310,15 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     if (!(ok = mbar_wait(bars.p_full(t), (jg - 1) & 1, kWaitLimitNs))) break;
                     tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < kBlockN / 16; ++kk)
-                        mma_ts_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + kk * 128, dv_hi,
-                                    idO, (w.n_kv > 1 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < C::kPVSteps; ++kk) {
+                        const uint32_t boff = (kk * C::kPVKeys * 128) >> 4;
+                        if constexpr (FP8)
+                            mma_ts_f8_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + boff, dv_hi,
+                                           idO, (w.n_kv > 1 || kk > 0) ? 1u : 0u);
+                        else
+                            mma_ts_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + boff, dv_hi, idO,
+                                        (w.n_kv > 1 || kk > 0) ? 1u : 0u);
+                    }
                     mma_commit(bars.o_full(t));
                 }
                 if (ok) mma_commit(bars.empty(prev_v));
@@ -331,6 +358,9 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 continue;
             }
+            // exponent constant and LSE scale of this slice (E4M3 scales folded in)
+            const float c_u = FP8 ? scale_log2 * qs[w.bh] * ks[w.bh] : scale_log2;
+            const float scale_u = FP8 ? scale * qs[w.bh] * ks[w.bh] : scale;
             float m_ref = -INFINITY;  // reference max, unscaled units
             float l = 0.f;            // exp-sum relative to m_ref (fp32 terms; gives LSE)
             float lr = 0.f;           // the same sum over the bf16-rounded terms the MMA sees (normalises O)
@@ -374,31 +404,53 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const float mt =
                     fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
                 const float m_new = fmaxf(m_ref, mt);
-                const bool need = (m_new - m_ref) * scale_log2 > kRescaleLog2;  // true while m_ref = -inf
+                const bool need = (m_new - m_ref) * c_u > kRescaleLog2;  // true while m_ref = -inf
                 float alpha = 1.f;
                 if (need) {
-                    alpha = ex2((m_ref - m_new) * scale_log2);  // 0 on the first tile
+                    alpha = ex2((m_ref - m_new) * c_u);  // 0 on the first tile
                     m_ref = m_new;
                 }
                 // P = exp2(s * scale * log2 e - m_ref * scale * log2 e), bf16, over the first 64 columns
                 // of S_t; fp32 and bf16-rounded row sums in independent partial accumulators
-                const float mc = (m_ref == -INFINITY ? 0.f : m_ref) * scale_log2;
-                const float2 c2 = make_float2(scale_log2, scale_log2), nmc2 = make_float2(-mc, -mc);
+                const float mc = (m_ref == -INFINITY ? 0.f : m_ref) * c_u;
+                const float2 c2 = make_float2(c_u, c_u), nmc2 = make_float2(-mc, -mc);
                 float2 lf[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                 make_float2(0.f, 0.f)};
                 float lq[4] = {0.f, 0.f, 0.f, 0.f};
+                if constexpr (FP8) {
+                    // P rounded to E4M3, four per tensor-memory column (128 keys -> 32 columns)
+                    uint32_t pw[32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t p[16];
+                    for (int i = 0; i < 32; ++i) {
+                        const float2 x01 = fma2(make_float2(s[4 * i], s[4 * i + 1]), c2, nmc2);
+                        const float2 x23 = fma2(make_float2(s[4 * i + 2], s[4 * i + 3]), c2, nmc2);
+                        const float p0 = ex2(x01.x), p1 = ex2(x01.y), p2 = ex2(x23.x), p3 = ex2(x23.y);
+                        lf[i & 3] = add2(lf[i & 3], add2(make_float2(p0, p1), make_float2(p2, p3)));
+                        pw[i] = pack_e4m3x4(p0, p1, p2, p3);
+                        lq[i & 3] = add_e4m3x4(lq[i & 3], pw[i]);
+                    }
+                    uint32_t h0[16], h1[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float2 x = fma2(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), c2, nmc2);
-                        const float p0 = ex2(x.x), p1 = ex2(x.y);
-                        lf[i & 3] = add2(lf[i & 3], make_float2(p0, p1));
-                        p[i] = pack_bf16x2(p0, p1);
-                        lq[i & 3] = add_bf16x2(lq[i & 3], p[i]);
+                        h0[i] = pw[i];
+                        h1[i] = pw[16 + i];
                     }
-                    tmem_st16(tS + c * 16, p);
+                    tmem_st16(tS, h0);
+                    tmem_st16(tS + 16, h1);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t p[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float2 x = fma2(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), c2, nmc2);
+                            const float p0 = ex2(x.x), p1 = ex2(x.y);
+                            lf[i & 3] = add2(lf[i & 3], make_float2(p0, p1));
+                            p[i] = pack_bf16x2(p0, p1);
+                            lq[i & 3] = add_bf16x2(lq[i & 3], p[i]);
+                        }
+                        tmem_st16(tS + c * 16, p);
+                    }
                 }
                 const float2 lf01 = add2(lf[0], lf[1]), lf23 = add2(lf[2], lf[3]);
                 const float2 lfs = add2(lf01, lf23);
@@ -436,7 +488,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // error.  The next unit's first P V (which overwrites O_t) is issued
             // only after this warpgroup's next p_full arrive, so the reads here are safe.
             // a row with no admitted key in this split has l = 0: O = 0, LSE = -inf
-            const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
+            const float inv_l = lr > 0.f ? (FP8 ? vs[w.bh] : 1.f) / lr : 0.f;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
@@ -463,7 +515,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                 }
             }
-            if (row_g < N) lse[out_row] = l > 0.f ? m_ref * scale + logf(l) : -INFINITY;
+            if (row_g < N) lse[out_row] = l > 0.f ? m_ref * scale_u + logf(l) : -INFINITY;
             ++uc;
         }
         if (!ok) report_timeout();
@@ -499,29 +551,33 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// [BH][N][d] bf16 viewed as a 3-D tensor (d fastest); box = 64 columns x 128 rows x 1 slice.
-bool make_map(CUtensorMap *m, const void *base, int64_t BH, int64_t N, int d)
+// [BH][N][d] (bf16, or E4M3 as bytes) viewed as a 3-D tensor (d fastest);
+// box = 128 bytes of columns x 128 rows x 1 slice.
+bool make_map(CUtensorMap *m, const void *base, int64_t BH, int64_t N, int d, int elem = 2)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elem, static_cast<cuuint64_t>(N) * d * elem};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem), 128, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return fn(m, elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool CAUSAL, bool OUT_F32>
-cudaError_t launch(const FaProblem &p, void *o, float *lse, int n_splits, int kv_chunk, cudaStream_t stream)
+template <int D, bool CAUSAL, bool OUT_F32, bool FP8 = false>
+cudaError_t launch(const FaProblem &p, void *o, float *lse, int n_splits, int kv_chunk, cudaStream_t stream,
+                   const float *qs = nullptr, const float *ks = nullptr, const float *vs = nullptr)
 {
-    using C = Cfg<D>;
+    using C = Cfg<D, FP8>;
     CUtensorMap mq, mk, mv;
     const int64_t BH = p.B * p.H;
-    if (!make_map(&mq, p.q, BH, p.N, D) || !make_map(&mk, p.k, BH, p.N, D) || !make_map(&mv, p.v, BH, p.N, D))
+    if (!make_map(&mq, p.q, BH, p.N, D, C::kElem) || !make_map(&mk, p.k, BH, p.N, D, C::kElem) ||
+        !make_map(&mv, p.v, BH, p.N, D, C::kElem))
         return cudaErrorInvalidValue;
-    auto kern = fa_fwd_tc_kernel<D, CAUSAL, OUT_F32>;
+    auto kern = fa_fwd_tc_kernel<D, CAUSAL, OUT_F32, FP8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t n_mblocks = (p.N + kQTiles * kBlockM - 1) / (kQTiles * kBlockM);
@@ -531,7 +587,7 @@ cudaError_t launch(const FaProblem &p, void *o, float *lse, int n_splits, int kv
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
     kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
         mq, mk, mv, o, lse, static_cast<int>(p.N), static_cast<int>(BH), static_cast<int>(n_mblocks),
-        static_cast<int>(n_units), n_splits, kv_chunk, p.scale, scale_log2);
+        static_cast<int>(n_units), n_splits, kv_chunk, p.scale, scale_log2, qs, ks, vs);
     return cudaGetLastError();
 }
 
@@ -556,6 +612,14 @@ cudaError_t fa_launch_tc_partials(const FaProblem &p, float *o_parts, float *lse
                                   cudaStream_t stream)
 {
     return dispatch<true>(p, o_parts, lse_parts, n_splits, kv_chunk, stream);
+}
+
+cudaError_t fa_launch_tc_fp8(const FaProblem &p, const float *qs, const float *ks, const float *vs,
+                             cudaStream_t stream)
+{
+    if (p.d != 128) return cudaErrorInvalidValue;
+    return p.causal ? launch<128, true, false, true>(p, p.o, p.lse, 1, static_cast<int>(p.N), stream, qs, ks, vs)
+                    : launch<128, false, false, true>(p, p.o, p.lse, 1, static_cast<int>(p.N), stream, qs, ks, vs);
 }
 
 int fa_tc_take_status(cudaStream_t stream)

@@ -22,6 +22,9 @@ cudaError_t fa_launch_tc(const FaProblem &p, cudaStream_t stream);
 // 128): split s writes fp32 O to o_parts + s*B*H*N*d and LSE to lse_parts + s*B*H*N.
 cudaError_t fa_launch_tc_partials(const FaProblem &p, float *o_parts, float *lse_parts, int n_splits, int kv_chunk,
                                   cudaStream_t stream);
+// The same kernel on E4M3 Q, K, V (d = 128) with per-(b, h) fp32 scales qs, ks, vs.
+cudaError_t fa_launch_tc_fp8(const FaProblem &p, const float *qs, const float *ks, const float *vs,
+                             cudaStream_t stream);
 // Merge of n_parts partial (O fp32, LSE) results of `rows` rows into bf16 O and LSE.
 cudaError_t fa_launch_combine(const float *o_parts, const float *lse_parts, int n_parts, int64_t rows, int d,
                               void *o, float *lse, int sm_count, cudaStream_t stream);

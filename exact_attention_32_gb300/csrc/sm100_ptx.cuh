@@ -221,6 +221,48 @@ __device__ __forceinline__ void mma_ts_lohi(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// Instruction descriptor, kind::f8f6f4 with E4M3 A and B, fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool b_mn_major)
+{
+    return (1u << 4)                                 // D format: f32
+           | (0u << 7)                               // A format: E4M3
+           | (0u << 10)                              // B format: E4M3
+           | ((b_mn_major ? 1u : 0u) << 16)          // B major-ness
+           | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
+}
+
+// kind::f8f6f4 forms of the two MMAs (K = 32 8-bit elements per instruction).
+__device__ __forceinline__ void mma_ss_f8_lohi(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                               uint32_t b_hi, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        ".reg .b64 da, db;\n"
+        "mov.b64 da, {%1, %2};\n"
+        "mov.b64 db, {%3, %4};\n"
+        "setp.ne.b32 p, %6, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_f8_lohi(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                               uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        ".reg .b64 db;\n"
+        "mov.b64 db, {%2, %3};\n"
+        "setp.ne.b32 p, %5, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %4, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate)
@@ -364,6 +406,32 @@ __device__ __forceinline__ float add_bf16x2(float acc, uint32_t p)
 {
     asm("{\n.reg .b16 lo, hi;\nmov.b32 {lo, hi}, %1;\n"
         "add.rn.f32.bf16 %0, lo, %0;\nadd.rn.f32.bf16 %0, hi, %0;\n}\n"
+        : "+f"(acc)
+        : "r"(p));
+    return acc;
+}
+
+// Four fp32 -> packed E4M3 (round to nearest even, saturating to +-448);
+// v0 in the lowest byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float v0, float v1, float v2, float v3)
+{
+    uint32_t lo, hi;
+    asm("{\n.reg .b16 t;\ncvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\ncvt.u32.u16 %0, t;\n}\n"
+        : "=r"(lo) : "f"(v0), "f"(v1));
+    asm("{\n.reg .b16 t;\ncvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\ncvt.u32.u16 %0, t;\n}\n"
+        : "=r"(hi) : "f"(v2), "f"(v3));
+    return lo | (hi << 16);
+}
+
+// acc + the four E4M3 values of a packed word, in fp32 (decoded exactly through f16).
+__device__ __forceinline__ float add_e4m3x4(float acc, uint32_t p)
+{
+    asm("{\n.reg .b16 b0, b1;\n.reg .b32 h0, h1;\n.reg .b16 f0, f1, f2, f3;\n"
+        "mov.b32 {b0, b1}, %1;\n"
+        "cvt.rn.f16x2.e4m3x2 h0, b0;\ncvt.rn.f16x2.e4m3x2 h1, b1;\n"
+        "mov.b32 {f0, f1}, h0;\nmov.b32 {f2, f3}, h1;\n"
+        "add.rn.f32.f16 %0, f0, %0;\nadd.rn.f32.f16 %0, f1, %0;\n"
+        "add.rn.f32.f16 %0, f2, %0;\nadd.rn.f32.f16 %0, f3, %0;\n}\n"
         : "+f"(acc)
         : "r"(p));
     return acc;

@@ -94,6 +94,19 @@ def make_grad_output(B: int, H: int, N: int, d: int, seed: int, device="cpu"):
     return t.to(device) if str(device) != "cpu" else t
 
 
+def quantize_e4m3(t: torch.Tensor):
+    """Encode a [B, H, N, d] tensor as E4M3 with one power-of-two fp32 scale per
+    (b, h): scale = 2^ceil(log2(absmax / 448)), t8 = round_to_e4m3(t / scale).
+    Returns (t8 float8_e4m3fn, scale fp32 [B, H], dequantised bf16 t8 * scale).
+    With a power-of-two scale the dequantised values are exact in bf16."""
+    a = t.float().abs().amax(dim=(-1, -2))
+    a = torch.where(a > 0, a, torch.ones_like(a))
+    scale = torch.exp2(torch.ceil(torch.log2(a / 448.0)))
+    t8 = (t.float() / scale[..., None, None]).to(torch.float8_e4m3fn)
+    deq = (t8.float() * scale[..., None, None]).to(torch.bfloat16)
+    return t8, scale.contiguous(), deq
+
+
 def workload_inputs(w: Workload, device="cpu", seed=None):
     """Inputs of a named workload (its own seed unless one is given)."""
     return make_inputs(w.B, w.H, w.N, w.d, w.seed if seed is None else seed,

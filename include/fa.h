@@ -162,6 +162,27 @@ int fa_combine(const float *o_parts, const float *lse_parts, int64_t n_parts, vo
                float *lse, int64_t B, int64_t H, int64_t N, int64_t d, void *stream);
 
 /*
+ * fa_fwd_fp8 - the forward of fa_fwd on 8-bit inputs ("FlashAttention: IO-Aware
+ * Tiling, ...", section "FlashAttention-3": FP8 E4M3 with block quantisation
+ * and scaling factors; the page fixes no scale policy, so here the block is
+ * one (b, h) slice).  The real inputs are q_scale[b*H + h] * q8 (and the same
+ * for k, v): S = scale * q_scale * k_scale * q8 k8^T, P = softmax(S), and P is
+ * rounded to E4M3 for the P V product, O = v_scale * P v8.
+ *
+ *   q, k, v   : const E4M3 bytes, contiguous [B, H, N, d]
+ *   q_scale, k_scale, v_scale : const fp32 [B*H], finite and > 0
+ *   o         : bf16 out [B, H, N, d];  lse : fp32 out [B, H, N]
+ *   d         : 128 only (else FA_ERR_UNSUPPORTED)
+ * Other arguments and errors as fa_fwd.  Accuracy is set by E4M3's 3-bit
+ * mantissa on P (O is divided by the sum of the rounded P, so the weights
+ * still sum to one); LSE uses the unrounded sum.
+ */
+int fa_fwd_fp8(const void *q, const void *k, const void *v, const float *q_scale,
+               const float *k_scale, const float *v_scale, void *o, float *lse,
+               int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
+               void *stream);
+
+/*
  * fa_bwd - gradients of sum(O * dO) with respect to Q, K and V for the
  * attention fa_fwd computes ("6.1 FlashAttention V1 in detail", section 6:
  * dV = P^T dO, dP = dO V^T, D = rowsum(dO * O), dS = P * (dP - D); and

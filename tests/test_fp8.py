@@ -1,0 +1,83 @@
+"""E4M3 forward (fa_fwd_fp8) against the fp64 oracle.
+
+Inputs are the seeded bf16 workloads encoded per (b, h) with power-of-two
+scales (exact dequantisation), so the oracle runs on exactly the values the
+kernel multiplies.  The only approximation left is P rounded to E4M3 (3-bit
+mantissa, relative half-step 2^-4) for the P V product; a CPU simulation of
+that rounding on these workloads gives max |dO| up to 0.06 and mean |dO| up
+to 0.004, hence (with about a factor of two):
+    max |dO| <= 0.12,  mean |dO| <= 1e-2,  max |dLSE| <= 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_32_gb300 import WORKLOADS, fa_get_device_status, forward_fp8, make_inputs, workload_inputs
+from exact_attention_32_gb300.workloads import quantize_e4m3, sample_rows
+
+MAX_O, MEAN_O, MAX_LSE = 0.12, 1e-2, 1e-3
+
+
+def test_quantization_is_exact_in_bf16():
+    q, _, _ = make_inputs(2, 3, 100, 128, seed=1, q_gain=8.0)
+    q8, s, deq = quantize_e4m3(q)
+    assert q8.dtype == torch.float8_e4m3fn and s.shape == (2, 3)
+    assert torch.all(torch.log2(s) == torch.round(torch.log2(s)))
+    assert torch.equal(deq.double(), q8.double() * s.double()[..., None, None])
+    assert (q8.float().abs().amax(dim=(-1, -2)) <= 448).all()
+
+
+def run(q, k, v, scale, causal):
+    (q8, qs, qd), (k8, ks, kd), (v8, vs, vd) = (quantize_e4m3(t) for t in (q, k, v))
+    o, lse = forward_fp8(q8.cuda(), k8.cuda(), v8.cuda(), qs.cuda(), ks.cuda(), vs.cuda(), scale=scale,
+                         causal=causal)
+    torch.cuda.synchronize()
+    assert fa_get_device_status(0) == 0
+    return o.double().cpu().numpy(), lse.double().cpu().numpy(), (qd, kd, vd)
+
+
+def check(o, lse, o_ref, lse_ref):
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    e, le = np.abs(o - o_ref), np.abs(lse - lse_ref)
+    assert e.max() <= MAX_O and e.mean() <= MEAN_O and le.max() <= MAX_LSE, (e.max(), e.mean(), le.max())
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 127, 128, 129, 256, 300, 1000])
+def test_small_problems_every_row(N, causal):
+    q, k, v = make_inputs(2, 2, N, 128, seed=4000 + N + causal)
+    scale = float(np.float32(1 / np.sqrt(128)))
+    o, lse, (qd, kd, vd) = run(q, k, v, scale, causal)
+    o_ref, lse_ref = oracle.attention(qd, kd, vd, scale, causal)
+    check(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["b4_h16_n2048_d128", "b2_h32_n4096_d128_causal", "b1_h32_n16384_d128_causal"])
+def test_workloads_sampled_rows(name):
+    w = WORKLOADS[name]
+    q, k, v = workload_inputs(w)
+    o, lse, (qd, kd, vd) = run(q, k, v, w.scale, w.causal)
+    rows = sample_rows(w.B, w.H, w.N, per_head=16, seed=w.seed)
+    o_ref, lse_ref = oracle.attention(qd, kd, vd, w.scale, w.causal, rows=rows)
+    check(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref)
+
+
+@pytest.mark.gpu
+def test_large_logits():
+    q, k, v = make_inputs(1, 4, 1000, 128, seed=4100, q_gain=8.0)
+    o, lse, (qd, kd, vd) = run(q, k, v, 0.0883883461356163, True)
+    o_ref, lse_ref = oracle.attention(qd, kd, vd, 0.0883883461356163, True)
+    check(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.gpu
+def test_head_dim_64_unsupported():
+    import exact_attention_32_gb300 as fa
+    q8 = torch.zeros((1, 1, 128, 64), dtype=torch.uint8, device="cuda")
+    s = torch.ones(1, device="cuda")
+    with pytest.raises(fa.FAError) as e:
+        fa.forward_fp8(q8, q8, q8, s, s, s)
+    assert e.value.status == 2
