@@ -30,6 +30,10 @@ Independent references, each in fp64 or better:
                        llms.blog page, section "Backward Pass Recomputation"
                        (dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d), with 1/sqrt(d)
                        read as the scale), dense per (b, h) slice.
+``attention_blocksparse`` the plain definition with a 0/1 block mask over
+                       (query block, key block) pairs: keys of a masked block
+                       take no part for the rows of that query block (numpy fp64,
+                       dense per slice).
 ``attention_decimal``  brute force in Python ``decimal`` at 50 digits, using
                        the softmax definition directly (exp(s_j) / sum exp(s_k),
                        no max shift) - an independent formulation for tiny
@@ -284,6 +288,41 @@ def attention_backward(q, k, v, do, scale: float, causal: bool, slices=None):
         out["lse"].append((m + np.log(l))[:, 0])
         out["D"].append(D[:, 0])
     return {name: np.stack(vals) for name, vals in out.items()}
+
+
+def attention_blocksparse(q, k, v, scale: float, causal: bool, block_mask, block: int = 128):
+    """fp64 attention restricted by a block mask ("FlashAttention: optimize data
+    movement before counting FLOPs", section 07, names the block-sparse variant;
+    the reading here: key j is admitted to query i only if
+    block_mask[i // block][j // block] is nonzero, and, when causal, j <= i).
+    Per slice: dense scores, masked entries -inf, the three-pass softmax of
+    the plain definition; a row with no admitted key gets O = 0, LSE = -inf.
+    block_mask: [ceil(N/block), ceil(N/block)] array, shared by all (b, h).
+    Returns (O [B, H, N, d], LSE [B, H, N]) float64."""
+    qd, kd, vd = _as_f64(q), _as_f64(k), _as_f64(v)
+    B, H, N, d = qd.shape
+    bm = np.asarray(block_mask).astype(bool)
+    nb = -(-N // block)
+    if bm.shape != (nb, nb):
+        raise ValueError("block_mask must be [ceil(N/block), ceil(N/block)]")
+    idx = np.arange(N) // block
+    allowed = bm[idx[:, None], idx[None, :]]
+    if causal:
+        allowed &= np.tril(np.ones((N, N), dtype=bool))
+    o = np.zeros((B, H, N, d))
+    lse = np.full((B, H, N), -np.inf)
+    live = allowed.any(axis=1)
+    for b in range(B):
+        for h in range(H):
+            S = scale * (qd[b, h] @ kd[b, h].T)
+            S[~allowed] = -np.inf
+            Sl = S[live]
+            m = Sl.max(axis=1, keepdims=True)        # pass 1
+            E = np.exp(Sl - m)
+            l = E.sum(axis=1, keepdims=True)         # pass 2
+            o[b, h, live] = (E / l) @ vd[b, h]       # pass 3
+            lse[b, h, live] = (m + np.log(l))[:, 0]
+    return o, lse
 
 
 def attention_decimal(q, k, v, scale, causal: bool, digits: int = 50):

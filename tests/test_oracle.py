@@ -382,3 +382,49 @@ def test_invalid_key_range_rejected():
     for r in [(2, 2), (-1, 3), (0, 5), (3, 1)]:
         with pytest.raises(ValueError):
             oracle.attention(q, k, v, 1.0, False, kv_range=r)
+
+
+# ------------------------------------------------------------------ block-sparse
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_blocksparse_all_ones_is_dense(causal):
+    q, k, v = make_inputs(1, 2, 300, 16, seed=41)
+    o, lse = oracle.attention_blocksparse(q, k, v, 0.25, causal, np.ones((3, 3)))
+    od, ld = oracle.attention(q, k, v, 0.25, causal)
+    assert np.allclose(o, od, rtol=1e-12, atol=1e-12) and np.allclose(lse, ld, rtol=1e-13, atol=1e-12)
+
+
+def test_blocksparse_block_diagonal_is_per_block_attention():
+    # a block-diagonal mask = independent attention inside each 128-row block
+    N, d = 384, 16
+    q, k, v = make_inputs(1, 2, N, d, seed=42)
+    o, lse = oracle.attention_blocksparse(q, k, v, 0.25, False, np.eye(3))
+    for b0 in range(0, N, 128):
+        sl = slice(b0, b0 + 128)
+        ob, lb = oracle.attention(q[:, :, sl].contiguous(), k[:, :, sl].contiguous(), v[:, :, sl].contiguous(),
+                                  0.25, False)
+        assert np.allclose(o[:, :, sl], ob, rtol=1e-12, atol=1e-12)
+        assert np.allclose(lse[:, :, sl], lb, rtol=1e-13, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_blocksparse_complementary_masks_merge_to_dense(causal):
+    # two masks that split the admitted blocks between them merge back to dense
+    rng = np.random.default_rng(7)
+    N = 500
+    nb = 4
+    m1 = rng.random((nb, nb)) < 0.5
+    q, k, v = make_inputs(1, 2, N, 8, seed=43, q_gain=2.0)
+    a = oracle.attention_blocksparse(q, k, v, 0.5, causal, m1)
+    b = oracle.attention_blocksparse(q, k, v, 0.5, causal, ~m1)
+    o, lse = oracle.merge([a[0], b[0]], [a[1], b[1]])
+    od, ld = oracle.attention(q, k, v, 0.5, causal)
+    assert np.allclose(o, od, rtol=1e-12, atol=1e-12) and np.allclose(lse, ld, rtol=1e-13, atol=1e-12)
+
+
+def test_blocksparse_row_without_blocks():
+    q, k, v = make_inputs(1, 1, 256, 8, seed=44)
+    mask = np.array([[1, 1], [0, 0]])
+    o, lse = oracle.attention_blocksparse(q, k, v, 0.5, False, mask)
+    assert np.all(o[:, :, 128:] == 0) and np.all(np.isneginf(lse[:, :, 128:]))
+    assert np.all(np.isfinite(lse[:, :, :128]))
