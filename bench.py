@@ -55,7 +55,7 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-secondary", action="store_true",
-                   help="skip the secondary rows: split-KV merge, backward and FP8 forward")
+                   help="skip the secondary rows: split-KV merge, backward, FP8 and block-sparse forward")
     return p.parse_args()
 
 
@@ -291,6 +291,54 @@ def fp8_throughput(w, dev, peaks, peak_src, steps=20):
             "launch_ms": ms}
 
 
+def blocksparse_throughput(w, dev, peaks, peak_src, steps=20):
+    """fa_fwd_blocksparse on the workload with a sliding window of three
+    128-blocks plus the first block column as global keys.  Algorithmic FLOPs:
+    4 d per admitted (query, key) pair (causal pairs only when causal)."""
+    import exact_attention_32_gb300 as fa
+    nb = -(-w.N // 128)
+    i, j = np.meshgrid(np.arange(nb), np.arange(nb), indexing="ij")
+    mask = ((np.abs(i - j) <= 1) | (j == 0)).astype(np.uint8)
+    # admitted pairs per slice, counted block by block (exact for causal diagonals)
+    pairs = 0
+    for qb in range(nb):
+        qlo, qhi = qb * 128, min(w.N, qb * 128 + 128)
+        for kb in np.nonzero(mask[qb])[0]:
+            klo, khi = kb * 128, min(w.N, kb * 128 + 128)
+            if not w.causal:
+                pairs += (qhi - qlo) * (khi - klo)
+            else:
+                for qi in range(qlo, qhi):
+                    pairs += max(0, min(khi, qi + 1) - klo)
+    flops = 4.0 * w.d * pairs * w.B * w.H
+    q, k, v = (t.to(dev) for t in workload_inputs(w))
+    bm = torch.as_tensor(mask, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, w.H, w.N, w.d,
+            w.scale, w.causal, bm.data_ptr(), stream.cuda_stream)
+    for _ in range(3):
+        st = fa.fa_fwd_blocksparse(*args)
+        if st != 0:
+            raise fa.FAError(st, "fa_fwd_blocksparse")
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fa.fa_fwd_blocksparse(*args)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    peak = float(peaks["bf16_tflops"])
+    achieved = flops / (ms / 1e3) / 1e12
+    return {"kernel": "fa_fwd_tc_kernel (block-sparse)", "row": "block-sparse forward",
+            "mask": "window of 3 blocks + first block column", "admitted_fraction_of_dense": flops / w.flops,
+            "bound": "tensor", "achieved": achieved, "peak": peak,
+            "peak_source": f"{peak_src} bf16_tflops (burst)", "unit": "TFLOP/s", "frac": achieved / peak,
+            "algorithmic_flops_per_launch": flops, "launch_ms": ms}
+
+
 # ------------------------------------------------------------- CPU baseline
 
 def oracle_rows_for(w, seconds: float, threads: int, rng_seed: int = 0):
@@ -460,7 +508,7 @@ def run_ours(args, rank, world, local):
     line["clocks"] = clk
     if not args.no_secondary:
         sec = [combine_roofline(w, dev, peaks, peak_src), backward_throughput(w, dev, peaks, peak_src),
-               fp8_throughput(w, dev, peaks, peak_src)]
+               fp8_throughput(w, dev, peaks, peak_src), blocksparse_throughput(w, dev, peaks, peak_src)]
         line["secondary"] = [x for x in sec if x is not None]
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)

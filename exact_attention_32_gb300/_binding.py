@@ -24,7 +24,7 @@ FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_NO_DEVICE",
                 4: "FA_ERR_ARCH", 5: "FA_ERR_LAUNCH", 6: "FA_ERR_TIMEOUT", 7: "FA_ERR_WORKSPACE_LIMIT"}
 EXPORTED = ("fa_fwd", "fa_fwd_mma", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_combine",
-            "fa_fwd_splitkv_noalloc", "fa_fwd_fp8", "fa_bwd", "fa_bwd_workspace_bytes", "fa_get_device_status",
+            "fa_fwd_splitkv_noalloc", "fa_fwd_fp8", "fa_fwd_blocksparse", "fa_bwd", "fa_bwd_workspace_bytes", "fa_get_device_status",
             "fa_status_string", "fa_version")
 
 
@@ -57,6 +57,9 @@ def lib():
             L.fa_fwd_splitkv_noalloc.restype = ctypes.c_int
             L.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
                                                  ctypes.c_int, i64, vp]
+            L.fa_fwd_blocksparse.restype = ctypes.c_int
+            L.fa_fwd_blocksparse.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
+                                             ctypes.c_int, vp, vp]
             L.fa_fwd_fp8.restype = ctypes.c_int
             L.fa_fwd_fp8.argtypes = [vp] * 8 + [i64, i64, i64, i64, ctypes.c_float, ctypes.c_int, vp]
             L.fa_bwd.restype = ctypes.c_int
@@ -101,6 +104,12 @@ def fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, N, d, scale, causal, n_splits,
     device array: for callers that cannot allocate device memory."""
     return lib().fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), int(causal),
                                         n_splits, stream)
+
+
+def fa_fwd_blocksparse(q, k, v, o, lse, B, H, N, d, scale, causal, block_mask, stream) -> int:
+    """Raw call of the block-sparse forward (uint8 [nb][nb] device mask)."""
+    return lib().fa_fwd_blocksparse(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), int(causal),
+                                    block_mask, stream)
 
 
 def fa_fwd_fp8(q, k, v, qs, ks, vs, o, lse, B, H, N, d, scale, causal, stream) -> int:
@@ -278,4 +287,29 @@ def forward_fp8(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale: t
                         bool(causal), s.cuda_stream)
     if st != FA_OK:
         raise FAError(st, "fa_fwd_fp8")
+    return o, lse
+
+
+def forward_blocksparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_mask: torch.Tensor,
+                        scale: float | None = None, causal: bool = False,
+                        stream: torch.cuda.Stream | None = None):
+    """(O, LSE) by ``fa_fwd_blocksparse``; block_mask is a 0/1 tensor
+    [ceil(N/128), ceil(N/128)] (moved to the device as uint8)."""
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.shape != q.shape:
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors of one shape")
+    B, H, N, d = q.shape
+    nb = -(-N // 128)
+    if tuple(block_mask.shape) != (nb, nb):
+        raise ValueError(f"block_mask must be [{nb}, {nb}]")
+    bm = (block_mask != 0).to(device=q.device, dtype=torch.uint8).contiguous()
+    scale = default_scale(d) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        st = fa_fwd_blocksparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                B, H, N, d, float(scale), bool(causal), bm.data_ptr(), s.cuda_stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_blocksparse")
     return o, lse

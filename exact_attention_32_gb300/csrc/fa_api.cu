@@ -235,6 +235,43 @@ extern "C" int fa_combine(const float *o_parts, const float *lse_parts, int64_t 
     return FA_OK;
 }
 
+extern "C" int fa_fwd_blocksparse(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                                  int64_t H, int64_t N, int64_t d, float scale, int causal,
+                                  const uint8_t *block_mask, void *stream)
+{
+    int st = check_sizes(B, H, N, d);
+    if (st != FA_OK) return st;
+    if ((causal != 0 && causal != 1) || !(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+    int dev = 0, sm_count = 0;
+    if ((st = current_device(&dev, &sm_count)) != FA_OK) return st;
+    const void *ptrs[6] = {q, k, v, o, lse, block_mask};
+    for (const void *p : ptrs)
+        if ((st = check_pointer(p, dev)) != FA_OK) return st;
+    const uint64_t tbytes = static_cast<uint64_t>(B * H * N * d) * 2u;
+    const uint64_t lbytes = static_cast<uint64_t>(B * H * N) * 4u;
+    const uint64_t nb = static_cast<uint64_t>((N + 127) / 128);
+    if (overlaps(o, tbytes, lse, lbytes)) return FA_ERR_INVALID_ARG;
+    for (const void *in : {q, k, v, static_cast<const void *>(block_mask)}) {
+        const uint64_t ib = in == block_mask ? nb * nb : tbytes;
+        if (overlaps(o, tbytes, in, ib) || overlaps(lse, lbytes, in, ib)) return FA_ERR_INVALID_ARG;
+    }
+    FaProblem p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.lse = lse;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.d = static_cast<int>(d);
+    p.scale = scale;
+    p.causal = causal;
+    p.sm_count = sm_count;
+    if (fa_launch_tc_sparse(p, block_mask, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_LAUNCH;
+    return FA_OK;
+}
+
 extern "C" int fa_fwd_fp8(const void *q, const void *k, const void *v, const float *q_scale,
                           const float *k_scale, const float *v_scale, void *o, float *lse, int64_t B, int64_t H,
                           int64_t N, int64_t d, float scale, int causal, void *stream)

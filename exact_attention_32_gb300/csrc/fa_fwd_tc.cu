@@ -115,6 +115,15 @@ struct Unit {
     int bh, q_row0, split, kv_begin, kv_end, j0, n_kv;
 };
 
+// Block-sparse mode: K/V tile kj is processed for a unit when the block mask
+// admits it for either of the unit's two 128-row query blocks (a query block
+// past the last row admits nothing).
+__device__ __forceinline__ bool tile_live(const uint8_t *bm, int nb, int q_row0, int kj)
+{
+    const int qb = q_row0 / kBlockM;
+    return bm[qb * nb + kj] != 0 || (qb + 1 < nb && bm[(qb + 1) * nb + kj] != 0);
+}
+
 __device__ __forceinline__ int unit_index(int r)
 {
     const int G = gridDim.x, c = blockIdx.x;
@@ -145,12 +154,16 @@ __device__ __forceinline__ Unit unit_of(int u, int N, int BH, int n_mblocks, int
 // S MMAs see the raw E4M3 values and the scales are folded into the exponent
 // constant and the LSE; P is rounded to E4M3 for a kind::f8f6f4 P V MMA and vs
 // is applied in the epilogue.
-template <int D, bool CAUSAL, bool OUT_F32, bool FP8>
+// SPARSE: bm is a [nb][nb] 0/1 block mask (nb = ceil(N/128)) over (query block,
+// key block); K/V tiles no query block of the unit admits are skipped, and a
+// tile is fully masked for a query tile whose block does not admit it.
+template <int D, bool CAUSAL, bool OUT_F32, bool FP8, bool SPARSE>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, void *__restrict__ o, float *__restrict__ lse, int N,
                  int BH, int n_mblocks, int n_units, int n_splits, int kv_chunk, float scale, float scale_log2,
-                 const float *__restrict__ qs, const float *__restrict__ ks, const float *__restrict__ vs)
+                 const float *__restrict__ qs, const float *__restrict__ ks, const float *__restrict__ vs,
+                 const uint8_t *__restrict__ bm, int nb)
 {
     using C = Cfg<D, FP8>;
     extern __shared__ uint8_t smem_raw[];
@@ -162,6 +175,14 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kBarOffset + C::kNumBars * 8);
 
     const Bars<C::kStages> bars{bar0};
+    // K/V tiles a unit processes: all of its range, or in block-sparse mode those the mask admits
+    auto live = [&](const Unit &w, int j) { return !SPARSE || tile_live(bm, nb, w.q_row0, w.j0 + j); };
+    auto n_live = [&](const Unit &w) {
+        if (!SPARSE) return w.n_kv;
+        int n = 0;
+        for (int j = 0; j < w.n_kv; ++j) n += live(w, j) ? 1 : 0;
+        return n;
+    };
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // after a timeout anywhere (sticky until read by the host) CTAs do no work
     const bool run = *reinterpret_cast<volatile int *>(&g_tc_status) == 0;
@@ -202,7 +223,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             int it = 0, uc = 0;
             for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
                 const Unit w = unit_of<CAUSAL>(u, N, BH, n_mblocks, n_splits, kv_chunk);
-                if (w.n_kv == 0) continue;  // no admitted key: nothing to load
+                if (n_live(w) == 0) continue;  // no admitted key: nothing to load
                 // the Q buffers are free once the previous unit's last S MMAs have completed
                 if (!mbar_wait(bars.q_empty(), (uc & 1) ^ 1, kWaitLimitNs)) {
                     ok = false;
@@ -215,6 +236,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                     w.q_row0 + t * kBlockM, w.bh);
                 ++uc;
                 for (int j = 0; j < w.n_kv && ok; ++j) {
+                    if (!live(w, j)) continue;
                     for (int kind = 0; kind < 2; ++kind, ++it) {
                         const int slot = it % C::kStages, use = it / C::kStages;
                         if (!mbar_wait(bars.empty(slot), (use & 1) ^ 1, kWaitLimitNs)) {
@@ -255,12 +277,14 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             int it = 0, uc = 0, jg = 0;  // ring position, units done, K/V tiles done (all units)
             for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
                 const Unit w = unit_of<CAUSAL>(u, N, BH, n_mblocks, n_splits, kv_chunk);
-                if (w.n_kv == 0) continue;
+                if (n_live(w) == 0) continue;
                 if (!(ok = mbar_wait(bars.q_full(), uc & 1, kWaitLimitNs))) break;
                 tc_fence_after();
                 uint32_t prev_v_lo = 0;
                 int prev_v = -1;
-                for (int j = 0; j < w.n_kv && ok; ++j, ++jg) {
+                int jj = 0;  // K/V tiles of this unit processed so far
+                for (int j = 0; j < w.n_kv && ok; ++j) {
+                    if (!live(w, j)) continue;
                     const int kslot = it % C::kStages, kuse = it / C::kStages;
                     ++it;
                     const int vslot = it % C::kStages, vuse = it / C::kStages;
@@ -269,7 +293,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     tc_fence_after();
                     const uint32_t dk_lo = static_cast<uint32_t>(dk0) + kslot * kTile16;
                     for (int t = 0; t < kQTiles && ok; ++t) {
-                        if (j > 0) {
+                        if (jj > 0) {
                             if (!(ok = mbar_wait(bars.p_full(t), (jg - 1) & 1, kWaitLimitNs))) break;
                             tc_fence_after();
 #pragma unroll
@@ -277,10 +301,10 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                 const uint32_t boff = (kk * C::kPVKeys * 128) >> 4;
                                 if constexpr (FP8)
                                     mma_ts_f8_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + boff,
-                                                   dv_hi, idO, (j > 1 || kk > 0) ? 1u : 0u);
+                                                   dv_hi, idO, (jj > 1 || kk > 0) ? 1u : 0u);
                                 else
                                     mma_ts_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + boff,
-                                                dv_hi, idO, (j > 1 || kk > 0) ? 1u : 0u);
+                                                dv_hi, idO, (jj > 1 || kk > 0) ? 1u : 0u);
                             }
                         }
                         const uint32_t aq_lo = dq_lo + t * kTile16;
@@ -298,11 +322,13 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                     if (!ok) break;
                     mma_commit(bars.empty(kslot));
-                    if (j > 0) mma_commit(bars.empty(prev_v));
+                    if (jj > 0) mma_commit(bars.empty(prev_v));
                     if (!(ok = mbar_wait(bars.full(vslot), vuse & 1, kWaitLimitNs))) break;
                     tc_fence_after();
                     prev_v = vslot;
                     prev_v_lo = static_cast<uint32_t>(dv0) + vslot * kTile16;
+                    ++jg;
+                    ++jj;
                 }
                 if (!ok) break;
                 mma_commit(bars.q_empty());  // the last reads of this unit's Q are issued
@@ -314,10 +340,10 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         const uint32_t boff = (kk * C::kPVKeys * 128) >> 4;
                         if constexpr (FP8)
                             mma_ts_f8_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + boff, dv_hi,
-                                           idO, (w.n_kv > 1 || kk > 0) ? 1u : 0u);
+                                           idO, (jj > 1 || kk > 0) ? 1u : 0u);
                         else
                             mma_ts_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + boff, dv_hi, idO,
-                                        (w.n_kv > 1 || kk > 0) ? 1u : 0u);
+                                        (jj > 1 || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(bars.o_full(t));
                 }
@@ -342,8 +368,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const Unit w = unit_of<CAUSAL>(u, N, BH, n_mblocks, n_splits, kv_chunk);
             const int row_g = w.q_row0 + t * kBlockM + row;
             const int64_t out_row = (static_cast<int64_t>(w.split) * BH + w.bh) * N + row_g;
-            if (w.n_kv == 0) {
-                // no admitted key in this split: O = 0, LSE = -inf (no weight when merged)
+            if (n_live(w) == 0) {
+                // no admitted key in this split (or block mask): O = 0, LSE = -inf (no weight when merged)
                 if (row_g < N) {
                     if (OUT_F32) {
                         float4 *orow = reinterpret_cast<float4 *>(static_cast<float *>(o) + out_row * D);
@@ -364,7 +390,10 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             float m_ref = -INFINITY;  // reference max, unscaled units
             float l = 0.f;            // exp-sum relative to m_ref (fp32 terms; gives LSE)
             float lr = 0.f;           // the same sum over the bf16-rounded terms the MMA sees (normalises O)
-            for (int j = 0; j < w.n_kv; ++j, ++jg) {
+            const bool qb_ok = !SPARSE || (w.q_row0 / kBlockM + t < nb);
+            int jj = 0;  // K/V tiles of this unit processed so far
+            for (int j = 0; j < w.n_kv; ++j) {
+                if (!live(w, j)) continue;
                 if (!mbar_wait_warp(bars.s_full(t), jg & 1, kWaitLimitNs)) {
                     ok = false;
                     break;
@@ -382,6 +411,10 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
                 }
                 const int k0 = (w.j0 + j) * kBlockN;
+                if (SPARSE && (!qb_ok || bm[(w.q_row0 / kBlockM + t) * nb + w.j0 + j] == 0)) {
+#pragma unroll
+                    for (int i = 0; i < kBlockN; ++i) s[i] = -INFINITY;  // block not admitted for this query tile
+                }
                 const bool need_mask = k0 < w.kv_begin || k0 + kBlockN > w.kv_end ||
                                        (CAUSAL && k0 + kBlockN - 1 > w.q_row0 + t * kBlockM);
                 if (need_mask) {
@@ -456,9 +489,10 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const float2 lfs = add2(lf01, lf23);
                 l = l * alpha + (lfs.x + lfs.y);
                 lr = lr * alpha + ((lq[0] + lq[1]) + (lq[2] + lq[3]));
-                // numerator rescale u *= alpha (u holds P V up to tile j-1, complete: the
-                // commit that signalled S_t(j) was issued after that MMA); nothing to scale at j = 0
-                if (j > 0 && __any_sync(0xffffffffu, need)) {
+                // numerator rescale u *= alpha (u holds P V up to the previous tile, complete:
+                // the commit that signalled this S was issued after that MMA); nothing to
+                // scale on the unit's first tile
+                if (jj > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t r[32];
@@ -478,6 +512,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bars.p_full(t));
+                ++jg;
+                ++jj;
             }
             if (!ok || !(ok = mbar_wait_warp(bars.o_full(t), uc & 1, kWaitLimitNs))) break;
             tc_fence_after();
@@ -567,9 +603,10 @@ bool make_map(CUtensorMap *m, const void *base, int64_t BH, int64_t N, int d, in
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool CAUSAL, bool OUT_F32, bool FP8 = false>
+template <int D, bool CAUSAL, bool OUT_F32, bool FP8 = false, bool SPARSE = false>
 cudaError_t launch(const FaProblem &p, void *o, float *lse, int n_splits, int kv_chunk, cudaStream_t stream,
-                   const float *qs = nullptr, const float *ks = nullptr, const float *vs = nullptr)
+                   const float *qs = nullptr, const float *ks = nullptr, const float *vs = nullptr,
+                   const uint8_t *bm = nullptr)
 {
     using C = Cfg<D, FP8>;
     CUtensorMap mq, mk, mv;
@@ -577,7 +614,7 @@ cudaError_t launch(const FaProblem &p, void *o, float *lse, int n_splits, int kv
     if (!make_map(&mq, p.q, BH, p.N, D, C::kElem) || !make_map(&mk, p.k, BH, p.N, D, C::kElem) ||
         !make_map(&mv, p.v, BH, p.N, D, C::kElem))
         return cudaErrorInvalidValue;
-    auto kern = fa_fwd_tc_kernel<D, CAUSAL, OUT_F32, FP8>;
+    auto kern = fa_fwd_tc_kernel<D, CAUSAL, OUT_F32, FP8, SPARSE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t n_mblocks = (p.N + kQTiles * kBlockM - 1) / (kQTiles * kBlockM);
@@ -587,7 +624,8 @@ cudaError_t launch(const FaProblem &p, void *o, float *lse, int n_splits, int kv
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
     kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
         mq, mk, mv, o, lse, static_cast<int>(p.N), static_cast<int>(BH), static_cast<int>(n_mblocks),
-        static_cast<int>(n_units), n_splits, kv_chunk, p.scale, scale_log2, qs, ks, vs);
+        static_cast<int>(n_units), n_splits, kv_chunk, p.scale, scale_log2, qs, ks, vs, bm,
+        static_cast<int>((p.N + kBlockN - 1) / kBlockN));
     return cudaGetLastError();
 }
 
@@ -612,6 +650,20 @@ cudaError_t fa_launch_tc_partials(const FaProblem &p, float *o_parts, float *lse
                                   cudaStream_t stream)
 {
     return dispatch<true>(p, o_parts, lse_parts, n_splits, kv_chunk, stream);
+}
+
+cudaError_t fa_launch_tc_sparse(const FaProblem &p, const uint8_t *block_mask, cudaStream_t stream)
+{
+    const int N = static_cast<int>(p.N);
+    if (p.d == 64)
+        return p.causal ? launch<64, true, false, false, true>(p, p.o, p.lse, 1, N, stream, nullptr, nullptr, nullptr,
+                                                                 block_mask)
+                        : launch<64, false, false, false, true>(p, p.o, p.lse, 1, N, stream, nullptr, nullptr,
+                                                                  nullptr, block_mask);
+    return p.causal ? launch<128, true, false, false, true>(p, p.o, p.lse, 1, N, stream, nullptr, nullptr, nullptr,
+                                                              block_mask)
+                    : launch<128, false, false, false, true>(p, p.o, p.lse, 1, N, stream, nullptr, nullptr, nullptr,
+                                                               block_mask);
 }
 
 cudaError_t fa_launch_tc_fp8(const FaProblem &p, const float *qs, const float *ks, const float *vs,

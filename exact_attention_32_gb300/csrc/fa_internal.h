@@ -22,6 +22,8 @@ cudaError_t fa_launch_tc(const FaProblem &p, cudaStream_t stream);
 // 128): split s writes fp32 O to o_parts + s*B*H*N*d and LSE to lse_parts + s*B*H*N.
 cudaError_t fa_launch_tc_partials(const FaProblem &p, float *o_parts, float *lse_parts, int n_splits, int kv_chunk,
                                   cudaStream_t stream);
+// The same kernel restricted by a [ceil(N/128)]^2 0/1 block mask over (query block, key block).
+cudaError_t fa_launch_tc_sparse(const FaProblem &p, const uint8_t *block_mask, cudaStream_t stream);
 // The same kernel on E4M3 Q, K, V (d = 128) with per-(b, h) fp32 scales qs, ks, vs.
 cudaError_t fa_launch_tc_fp8(const FaProblem &p, const float *qs, const float *ks, const float *vs,
                              cudaStream_t stream);

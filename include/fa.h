@@ -162,6 +162,23 @@ int fa_combine(const float *o_parts, const float *lse_parts, int64_t n_parts, vo
                float *lse, int64_t B, int64_t H, int64_t N, int64_t d, void *stream);
 
 /*
+ * fa_fwd_blocksparse - fa_fwd restricted by a block mask ("FlashAttention:
+ * optimize data movement before counting FLOPs", section 07, names the
+ * block-sparse variant without defining it; here): key j is admitted to
+ * query i only if block_mask[(i / 128) * nb + j / 128] != 0, nb = ceil(N/128),
+ * and, when causal, j <= i.  K/V tiles no query block of a work unit admits
+ * are never loaded or multiplied.  A row that admits no key gets O = 0 and
+ * LSE = -inf.
+ *
+ *   block_mask : const uint8 [nb][nb] device array (row = query block), shared
+ *                by every (b, h); 16-byte aligned like the other pointers.
+ * Other arguments and errors as fa_fwd.
+ */
+int fa_fwd_blocksparse(const void *q, const void *k, const void *v, void *o, float *lse,
+                       int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
+                       const uint8_t *block_mask, void *stream);
+
+/*
  * fa_fwd_fp8 - the forward of fa_fwd on 8-bit inputs ("FlashAttention: IO-Aware
  * Tiling, ...", section "FlashAttention-3": FP8 E4M3 with block quantisation
  * and scaling factors; the page fixes no scale policy, so here the block is
