@@ -16,7 +16,8 @@
 //                         the 128-row query blocks (causal: from the diagonal);
 //                         dK, dV accumulate in tensor memory, dQ block partials
 //                         are added into the fp32 accumulator.
-//   post  (memory-bound)  dQ = bf16(scale * accumulator).
+//   post  (memory-bound)  dQ = bf16(scale * accumulator), from the blocked
+//                         accumulator layout below back to [B, H, N, d].
 //
 // Main kernel, per query block (S^T etc. are key-major: TMEM lane = key):
 //   S^T  = K Q^T          SS MMA -> TMEM A
@@ -27,7 +28,17 @@
 //                                                 into shared memory (for dQ)
 //   dK  += dS^T Q         TS MMA -> TMEM D
 //   dQ   = dS K           SS MMA (A = dS MN-major, B = K MN-major) -> TMEM A,
-//                         read back and added to the accumulator (red.v4.f32)
+//                         read into registers (TMEM A is released at once) and
+//                         staged in the Q/dO stage that block no longer needs;
+//                         the load warp adds the staged block to the
+//                         accumulator with one bulk reduce-add, waits until
+//                         it has been read out and refills the stage
+// The dQ accumulator is blocked: one 128 x d fp32 block per (b, h, query
+// block), holding the block's 8 warp slices (warpgroup, 32-row group) one after
+// the other, each 32 rows x d/2 columns, row-major, with the 16-byte chunk c of
+// row l stored at chunk position c ^ (l mod d/8).  A warp's slice is then one
+// contiguous range of global memory, and its staging writes in shared memory
+// are free of bank conflicts.
 // Roles (320 threads): warps 0-3 and 4-7 are two warpgroups that take query
 // columns 0-63 and 64-127 of each block (and d-columns halves of dQ, dK, dV);
 // warp 8 loads K, V once and Q, dO, LSE, D per block (two stages); warp 9
@@ -76,7 +87,7 @@ struct BCfg {
     static constexpr int kSmemBytes = kBar + kNumBars * 8 + 16;
 };
 
-enum { KV_FULL = 0, Q_FULL = 1, Q_EMPTY = 3, S_FULL = 5, DP_FULL = 6, P_READY = 7, DS_READY = 8, DQ_FULL = 9,
+enum { KV_FULL = 0, Q_FULL = 1, DQ_STAGED = 3, S_FULL = 5, DP_FULL = 6, P_READY = 7, DS_READY = 8, DQ_FULL = 9,
        DQ_CONSUMED = 10, DONE = 11, MMA_DONE = 12 };
 
 __device__ __forceinline__ uint32_t lo32(uint64_t x) { return static_cast<uint32_t>(x); }
@@ -117,7 +128,7 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         mbar_init(BAR(KV_FULL), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(BAR(Q_FULL + s), 1);
-            mbar_init(BAR(Q_EMPTY + s), 1);
+            mbar_init(BAR(DQ_STAGED + s), 8);  // the softmax warps, once their dQ slices are staged
         }
         mbar_init(BAR(S_FULL), 1);
         mbar_init(BAR(DP_FULL), 1);
@@ -153,13 +164,21 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tma_load_3d(sb + C::kK + a * 16384, &tm_k, BAR(KV_FULL), a * 64, k0, bh);
                 tma_load_3d(sb + C::kV + a * 16384, &tm_v, BAR(KV_FULL), a * 64, k0, bh);
             }
+            // add the dQ block that iteration j staged in stage j & 1 to the accumulator
+            auto flush = [&](int j) -> bool {
+                if (!mbar_wait(BAR(DQ_STAGED + (j & 1)), (j >> 1) & 1, kWaitLimitNs)) return false;
+                bulk_reduce_add_f32(dq_acc + (static_cast<int64_t>(bh) * n_blocks + qb0 + j) * (kBlock * D),
+                                    sb + C::kStage0 + (j & 1) * C::kStageBytes, kBlock * D * 4);
+                bulk_commit();
+                return true;
+            };
             bool ok = true;
             int issued = 0;
             for (int i = 0; i < nq; ++i) {
                 const int st = i & 1;
-                if (!mbar_wait(BAR(Q_EMPTY + st), ((i >> 1) & 1) ^ 1, kWaitLimitNs)) {
-                    ok = false;
-                    break;
+                if (i >= 2) {  // the stage is free once the block staged in it two iterations ago is read out
+                    if (!(ok = flush(i - 2))) break;
+                    bulk_wait_read0();
                 }
                 const int q0 = (qb0 + i) * kBlock;
                 const uint32_t sq = sb + C::kStage0 + st * C::kStageBytes, sdo = sq + C::kTile;
@@ -173,6 +192,8 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 bulk_load(sb + C::kVec + st * 1024 + 512, dvec + vo, 512, BAR(Q_FULL + st));
                 ++issued;
             }
+            for (int j = nq >= 2 ? nq - 2 : 0; j < nq && ok; ++j) ok = flush(j);
+            bulk_wait0();  // the accumulator additions complete before the CTA ends
             if (!ok) report(FA_ERR_TIMEOUT);
             const uint64_t lim = ok ? kWaitLimitNs : kCleanupLimitNs;
             mbar_wait(BAR(KV_FULL), 0, lim);
@@ -233,7 +254,6 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     mma_ss_lohi(tA, lo32(d_ds_mn) + kk * 128, hi32(d_ds_mn), lo32(d_k_mn) + kk * 128, hi32(d_k_mn),
                                 idQ, kk > 0 ? 1u : 0u);
                 mma_commit(BAR(DQ_FULL));
-                mma_commit(BAR(Q_EMPTY + st));
             }
             if (ok) mma_commit(BAR(DONE));
             if (!ok) report(FA_ERR_TIMEOUT);
@@ -347,29 +367,36 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(DS_READY));
 
-            // dQ block partial: TMEM lane = query row; add into the fp32 accumulator
+            // dQ block partial (TMEM lane = query row): into registers, TMEM A released,
+            // then staged in this block's Q/dO stage (every MMA that read it has
+            // completed by DQ_FULL) for the load warp's bulk reduce
             if (!mbar_wait_warp(BAR(DQ_FULL), i & 1, kWaitLimitNs)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int qrow = q0 + r;
-            float *dst = dq_acc + (static_cast<int64_t>(bh) * N + qrow) * D + wg * (D / 2);
-#pragma unroll
-            for (int cc = 0; cc < D / 64; ++cc) {
-                uint32_t x[32];
-                tmem_ld32(tA + loff + wg * (D / 2) + cc * 32, x);
-                tmem_wait_ld();
-                if (qrow < N) {
-#pragma unroll
-                    for (int k4 = 0; k4 < 8; ++k4)
-                        red_add_v4(dst + cc * 32 + 4 * k4, __uint_as_float(x[4 * k4]), __uint_as_float(x[4 * k4 + 1]),
-                                   __uint_as_float(x[4 * k4 + 2]), __uint_as_float(x[4 * k4 + 3]));
-                }
-            }
+            uint32_t x0[32], x1[32];
+            tmem_ld32(tA + loff + wg * (D / 2), x0);
+            if constexpr (D == 128) tmem_ld32(tA + loff + wg * (D / 2) + 32, x1);
+            tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(DQ_CONSUMED));
+            constexpr int kChunks = D / 8;               // 16-byte chunks in a row of the warp slice
+            constexpr int kSliceBytes = 32 * (D / 2) * 4;
+            const int slot = wg * 4 + (warp & 3);
+            const uint32_t stage_off = C::kStage0 + st * C::kStageBytes + slot * kSliceBytes;
+            uint8_t *srow = smem + stage_off + lane * (D * 2);
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) {
+                const uint32_t *x = c < 8 ? x0 : x1;
+                const int cl = c & 7;
+                *reinterpret_cast<uint4 *>(srow + ((c ^ (lane & (kChunks - 1))) * 16)) =
+                    make_uint4(x[4 * cl], x[4 * cl + 1], x[4 * cl + 2], x[4 * cl + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(DQ_STAGED + st));
         }
         if (ok) ok = mbar_wait_warp(BAR(DONE), 0, kWaitLimitNs);
         if (!ok) report(FA_ERR_TIMEOUT);
@@ -433,9 +460,6 @@ fa_bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__re
             for (int e = 0; e < PER; ++e) acc = fmaf(__bfloat162float(a[e]), __bfloat162float(b[e]), acc);
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            float *z = dq_acc + row * D + lane * PER;
-#pragma unroll
-            for (int e = 0; e < PER; ++e) z[e] = 0.f;
             if (lane == 0) {
                 dvec[rr] = acc;
                 lse2[rr] = lse[row] * 1.4426950408889634f;
@@ -444,16 +468,32 @@ fa_bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__re
             dvec[rr] = 0.f;
             lse2[rr] = INFINITY;
         }
+        // the accumulator holds B*H*n_pad*D floats: padded row rr clears floats [rr*D, rr*D + D)
+        float *z = dq_acc + rr * D + lane * PER;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) z[e] = 0.f;
     }
 }
 
-// dQ = bf16(scale * accumulator), four elements per thread.
+// dQ = bf16(scale * accumulator), four elements per thread; reads the blocked
+// accumulator layout described at the top of this file.
+template <int D>
 __global__ void __launch_bounds__(256)
-fa_bwd_post_kernel(const float4 *__restrict__ acc, uint2 *__restrict__ dq, int64_t n4, float scale)
+fa_bwd_post_kernel(const float4 *__restrict__ acc, uint2 *__restrict__ dq, int64_t n4, int N, int n_blocks,
+                   float scale)
 {
+    constexpr int kChunks = D / 8;  // 4-float chunks per half row
     for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n4;
          t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const float4 x = acc[t];
+        const int64_t row = t / (D / 4);
+        const int c4 = static_cast<int>(t - row * (D / 4));
+        const int64_t bh = row / N;
+        const int i = static_cast<int>(row - bh * N);
+        const int qb = i / kBlock, rr = i % kBlock;
+        const int slot = (c4 / kChunks) * 4 + rr / 32, l = rr % 32, c = c4 % kChunks;
+        const int64_t src = (bh * n_blocks + qb) * (kBlock * D / 4) + slot * (32 * kChunks) + l * kChunks +
+                            (c ^ (l & (kChunks - 1)));
+        const float4 x = acc[src];
         uint2 y;
         y.x = pack_bf16x2(x.x * scale, x.y * scale);
         y.y = pack_bf16x2(x.z * scale, x.w * scale);
@@ -524,14 +564,14 @@ cudaError_t launch_main(const FaBwdProblem &p, float *lse2, float *dvec, float *
 int64_t fa_bwd_workspace_size(int64_t B, int64_t H, int64_t N, int64_t d)
 {
     const int64_t n_pad = (N + kBlock - 1) / kBlock * kBlock;
-    return B * H * N * d * 4 + 2 * B * H * n_pad * 4;
+    return B * H * n_pad * d * 4 + 2 * B * H * n_pad * 4;
 }
 
 cudaError_t fa_launch_bwd(const FaBwdProblem &p, void *workspace, cudaStream_t s)
 {
     const int64_t BH = p.B * p.H, n_pad = (p.N + kBlock - 1) / kBlock * kBlock;
     float *dq_acc = static_cast<float *>(workspace);
-    float *lse2 = dq_acc + BH * p.N * p.d;
+    float *lse2 = dq_acc + BH * n_pad * p.d;
     float *dvec = lse2 + BH * n_pad;
     // pre
     {
@@ -563,8 +603,15 @@ cudaError_t fa_launch_bwd(const FaBwdProblem &p, void *workspace, cudaStream_t s
         const int64_t n4 = BH * p.N * p.d / 4;
         const int64_t want = (n4 + 255) / 256, cap = static_cast<int64_t>(p.sm_count) * 16;
         const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-        fa_bwd_post_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4 *>(dq_acc),
-                                                 static_cast<uint2 *>(p.dq), n4, p.scale);
+        const int nb = static_cast<int>(n_pad / kBlock);
+        if (p.d == 64)
+            fa_bwd_post_kernel<64><<<grid, 256, 0, s>>>(reinterpret_cast<const float4 *>(dq_acc),
+                                                         static_cast<uint2 *>(p.dq), n4, static_cast<int>(p.N), nb,
+                                                         p.scale);
+        else
+            fa_bwd_post_kernel<128><<<grid, 256, 0, s>>>(reinterpret_cast<const float4 *>(dq_acc),
+                                                          static_cast<uint2 *>(p.dq), n4, static_cast<int>(p.N), nb,
+                                                          p.scale);
         return cudaGetLastError();
     }
 }
