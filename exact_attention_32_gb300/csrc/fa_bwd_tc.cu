@@ -103,7 +103,7 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                  const float *__restrict__ lse2, const float *__restrict__ dvec, float *__restrict__ dq_acc,
                  __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv, int N, int BH, int n_blocks,
-                 int n_pad, float scale, float scale_log2)
+                 int n_pad, int heads_per_group, float scale, float scale_log2)
 {
     using C = BCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -117,8 +117,14 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kBar + C::kNumBars * 8);
 
-    // CTA = key block kb of slice bh; causal blocks with many query blocks (small kb) first
-    const int kb = blockIdx.x / BH, bh = blockIdx.x % BH;
+    // CTA = key block kb of slice bh.  The (b, h) slices go in groups of
+    // heads_per_group, so that the CTAs resident at one time share a few
+    // slices' Q, dO and dQ accumulator blocks in L2; inside a group, key-block
+    // major, so causal CTAs with many query blocks (small kb) start first.
+    const int per_group = heads_per_group * n_blocks;
+    const int grp = blockIdx.x / per_group, rem = blockIdx.x - grp * per_group;
+    const int gsize = min(heads_per_group, BH - grp * heads_per_group);
+    const int kb = rem / gsize, bh = grp * heads_per_group + rem % gsize;
     const int k0 = kb * kBlock;
     const int qb0 = CAUSAL ? kb : 0;
     const int nq = n_blocks - qb0;
@@ -553,9 +559,12 @@ cudaError_t launch_main(const FaBwdProblem &p, float *lse2, float *dvec, float *
     const int64_t grid = n_blocks * BH;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
+    // about 256 CTAs per group of slices (at least one slice)
+    const int64_t hpg = n_blocks >= 256 ? 1 : (256 / n_blocks < BH ? 256 / n_blocks : BH);
     kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, s>>>(
         mq, mk, mv, mdo, lse2, dvec, dq_acc, static_cast<__nv_bfloat16 *>(p.dk), static_cast<__nv_bfloat16 *>(p.dv),
-        static_cast<int>(p.N), static_cast<int>(BH), static_cast<int>(n_blocks), n_pad, p.scale, scale_log2);
+        static_cast<int>(p.N), static_cast<int>(BH), static_cast<int>(n_blocks), n_pad, static_cast<int>(hpg), p.scale,
+        scale_log2);
     return cudaGetLastError();
 }
 
