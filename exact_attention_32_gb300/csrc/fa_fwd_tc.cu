@@ -117,11 +117,29 @@ struct Unit {
 
 // Block-sparse mode: K/V tile kj is processed for a unit when the block mask
 // admits it for either of the unit's two 128-row query blocks (a query block
-// past the last row admits nothing).
-__device__ __forceinline__ bool tile_live(const uint8_t *bm, int nb, int q_row0, int kj)
+// past the last row admits nothing).  mask_word gives the tiles j0 + c .. j0 +
+// c + 31 of mask rows qa and qb as a bit mask (bit i: tile j0 + c + i admitted
+// by either row, tiles at or past j0 + n excluded); its 64 byte loads are
+// independent, so a word costs one memory round trip.
+__device__ __forceinline__ uint32_t mask_word(const uint8_t *__restrict__ bm, int nb, int qa, int qb, int j0, int c,
+                                              int n)
 {
-    const int qb = q_row0 / kBlockM;
-    return bm[qb * nb + kj] != 0 || (qb + 1 < nb && bm[(qb + 1) * nb + kj] != 0);
+    // every load is unconditional (addresses past the range are clamped to its
+    // last tile and their bits dropped below), so all 64 are in flight at once
+    const int last = n - 1 - c;  // >= 0: the caller asks only for words inside the range
+    const uint8_t *ra = bm + static_cast<int64_t>(qa) * nb + j0 + c;
+    const uint8_t *rb = bm + static_cast<int64_t>(qb) * nb + j0 + c;
+    uint32_t va[32], vb[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int k = i < last ? i : last;
+        va[i] = __ldg(ra + k);
+        vb[i] = __ldg(rb + k);
+    }
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m |= ((va[i] | vb[i]) != 0u ? 1u : 0u) << i;
+    return last >= 31 ? m : (m & ((2u << last) - 1u));
 }
 
 __device__ __forceinline__ int unit_index(int r)
@@ -175,13 +193,23 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kBarOffset + C::kNumBars * 8);
 
     const Bars<C::kStages> bars{bar0};
-    // K/V tiles a unit processes: all of its range, or in block-sparse mode those the mask admits
-    auto live = [&](const Unit &w, int j) { return !SPARSE || tile_live(bm, nb, w.q_row0, w.j0 + j); };
-    auto n_live = [&](const Unit &w) {
-        if (!SPARSE) return w.n_kv;
-        int n = 0;
-        for (int j = 0; j < w.n_kv; ++j) n += live(w, j) ? 1 : 0;
-        return n;
+    // K/V tiles a unit processes: all of its range, or in block-sparse mode those
+    // the mask admits for either query block of the unit.  In the tile loops,
+    // `word` holds the live bits of the 32-tile group of j (loaded at each group
+    // start) and j jumps to the group's next live tile, or past the group when
+    // none is left, so dead tiles cost no loop iterations.
+    auto unit_word = [&](const Unit &w, int c) {
+        const int qa = w.q_row0 / kBlockM, qb = qa + 1 < nb ? qa + 1 : qa;
+        return mask_word(bm, nb, qa, qb, w.j0, c, w.n_kv);
+    };
+    auto any_live = [&](const Unit &w) {
+        if constexpr (SPARSE) {
+            for (int c = 0; c < w.n_kv; c += 32)
+                if (unit_word(w, c) != 0) return true;
+            return false;
+        } else {
+            return w.n_kv > 0;
+        }
     };
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // after a timeout anywhere (sticky until read by the host) CTAs do no work
@@ -223,7 +251,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             int it = 0, uc = 0;
             for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
                 const Unit w = unit_of<CAUSAL>(u, N, BH, n_mblocks, n_splits, kv_chunk);
-                if (n_live(w) == 0) continue;  // no admitted key: nothing to load
+                if (!any_live(w)) continue;  // no admitted key: nothing to load
                 // the Q buffers are free once the previous unit's last S MMAs have completed
                 if (!mbar_wait(bars.q_empty(), (uc & 1) ^ 1, kWaitLimitNs)) {
                     ok = false;
@@ -235,8 +263,17 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &tm_q, bars.q_full(), a * (128 / C::kElem),
                                     w.q_row0 + t * kBlockM, w.bh);
                 ++uc;
+                uint32_t word = 0;
                 for (int j = 0; j < w.n_kv && ok; ++j) {
-                    if (!live(w, j)) continue;
+                    if constexpr (SPARSE) {
+                        if ((j & 31) == 0) word = unit_word(w, j);
+                        const uint32_t rest = word >> (j & 31);
+                        if (rest == 0) {
+                            j |= 31;
+                            continue;
+                        }
+                        j += __ffs(rest) - 1;
+                    }
                     for (int kind = 0; kind < 2; ++kind, ++it) {
                         const int slot = it % C::kStages, use = it / C::kStages;
                         if (!mbar_wait(bars.empty(slot), (use & 1) ^ 1, kWaitLimitNs)) {
@@ -277,14 +314,23 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             int it = 0, uc = 0, jg = 0;  // ring position, units done, K/V tiles done (all units)
             for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
                 const Unit w = unit_of<CAUSAL>(u, N, BH, n_mblocks, n_splits, kv_chunk);
-                if (n_live(w) == 0) continue;
+                if (!any_live(w)) continue;
                 if (!(ok = mbar_wait(bars.q_full(), uc & 1, kWaitLimitNs))) break;
                 tc_fence_after();
                 uint32_t prev_v_lo = 0;
                 int prev_v = -1;
                 int jj = 0;  // K/V tiles of this unit processed so far
+                uint32_t word = 0;
                 for (int j = 0; j < w.n_kv && ok; ++j) {
-                    if (!live(w, j)) continue;
+                    if constexpr (SPARSE) {
+                        if ((j & 31) == 0) word = unit_word(w, j);
+                        const uint32_t rest = word >> (j & 31);
+                        if (rest == 0) {
+                            j |= 31;
+                            continue;
+                        }
+                        j += __ffs(rest) - 1;
+                    }
                     const int kslot = it % C::kStages, kuse = it / C::kStages;
                     ++it;
                     const int vslot = it % C::kStages, vuse = it / C::kStages;
@@ -368,7 +414,25 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const Unit w = unit_of<CAUSAL>(u, N, BH, n_mblocks, n_splits, kv_chunk);
             const int row_g = w.q_row0 + t * kBlockM + row;
             const int64_t out_row = (static_cast<int64_t>(w.split) * BH + w.bh) * N + row_g;
-            if (n_live(w) == 0) {
+            const bool qb_ok = !SPARSE || (w.q_row0 / kBlockM + t < nb);
+            // block-sparse: tiles j .. j+31 of the unit, one lane per tile.  Returns the
+            // tiles either query block admits; own_r gets those this warpgroup's block admits.
+            uint32_t own_r = 0;
+            auto load_words = [&](int j) -> uint32_t {
+                const int qa = w.q_row0 / kBlockM, qb2 = qa + 1 < nb ? qa + 1 : qa;
+                const bool in = j + lane < w.n_kv;
+                const int64_t kj = w.j0 + j + lane;
+                const uint8_t a = in ? __ldg(bm + qa * static_cast<int64_t>(nb) + kj) : 0;
+                const uint8_t b = in ? __ldg(bm + qb2 * static_cast<int64_t>(nb) + kj) : 0;
+                own_r = __ballot_sync(0xffffffffu, qb_ok && (t == 0 ? a : b) != 0);
+                return __ballot_sync(0xffffffffu, (a | b) != 0);
+            };
+            bool unit_live = w.n_kv > 0;
+            if constexpr (SPARSE) {
+                unit_live = false;
+                for (int c = 0; c < w.n_kv && !unit_live; c += 32) unit_live = load_words(c) != 0;
+            }
+            if (!unit_live) {
                 // no admitted key in this split (or block mask): O = 0, LSE = -inf (no weight when merged)
                 if (row_g < N) {
                     if (OUT_F32) {
@@ -390,10 +454,15 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             float m_ref = -INFINITY;  // reference max, unscaled units
             float l = 0.f;            // exp-sum relative to m_ref (fp32 terms; gives LSE)
             float lr = 0.f;           // the same sum over the bf16-rounded terms the MMA sees (normalises O)
-            const bool qb_ok = !SPARSE || (w.q_row0 / kBlockM + t < nb);
             int jj = 0;  // K/V tiles of this unit processed so far
+            uint32_t word = 0;  // block-sparse: live tiles of the 32-tile group of j
             for (int j = 0; j < w.n_kv; ++j) {
-                if (!live(w, j)) continue;
+                // block-sparse: dead tiles are stepped over one by one here (moving j
+                // inside this loop, as the producer and MMA loops do, costs spills)
+                if constexpr (SPARSE) {
+                    if ((j & 31) == 0) word = load_words(j);
+                    if (((word >> (j & 31)) & 1u) == 0) continue;
+                }
                 if (!mbar_wait_warp(bars.s_full(t), jg & 1, kWaitLimitNs)) {
                     ok = false;
                     break;
@@ -411,7 +480,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
                 }
                 const int k0 = (w.j0 + j) * kBlockN;
-                if (SPARSE && (!qb_ok || bm[(w.q_row0 / kBlockM + t) * nb + w.j0 + j] == 0)) {
+                if (SPARSE && (!qb_ok || ((own_r >> (j & 31)) & 1u) == 0)) {
 #pragma unroll
                     for (int i = 0; i < kBlockN; ++i) s[i] = -INFINITY;  // block not admitted for this query tile
                 }
