@@ -445,20 +445,20 @@ def run_ours(args, rank, world, local):
 
     value = w.flops * K * world / (total_ms / 1e3) / 1e12
 
-    # end to end through the public API: pinned host inputs in, O and LSE out
+    # end to end through the C ABI with host buffers (fa_fwd_host): pinned host
+    # Q, K, V in, O and LSE out, every copy inside the timed region; the
+    # library overlaps the copies of one group of (b, h) slices with the
+    # forward of another
     e2e = None
     if not args.no_e2e:
         qp, kp, vp_ = (t.pin_memory() for t in (q_h, k_h, v_h))
         op = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
         lp = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        staging = (q, k, v, o, lse)
 
         def e2e_step():
-            q.copy_(qp, non_blocking=True)
-            k.copy_(kp, non_blocking=True)
-            v.copy_(vp_, non_blocking=True)
-            fa.forward(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse)
-            op.copy_(o, non_blocking=True)
-            lp.copy_(lse, non_blocking=True)
+            fa.forward_host(qp, kp, vp_, scale=w.scale, causal=w.causal, out=op, lse=lp, staging=staging,
+                            device=dev, stream=stream)
 
         for _ in range(3):
             e2e_step()
@@ -476,7 +476,8 @@ def run_ours(args, rank, world, local):
         out_bytes = o.numel() * o.element_size() + lse.numel() * lse.element_size()
         e2e = {"value": w.flops * Ke * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
-               "steps": Ke, "ms_per_step": e2e_ms / Ke}
+               "steps": Ke, "ms_per_step": e2e_ms / Ke,
+               "api": "fa_fwd_host (pinned host buffers, copies overlapped over 4 groups of (b, h) slices)"}
 
     if rank != 0:
         return None

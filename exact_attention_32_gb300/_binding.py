@@ -23,7 +23,7 @@ _lock = threading.Lock()
 FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_NO_DEVICE",
                 4: "FA_ERR_ARCH", 5: "FA_ERR_LAUNCH", 6: "FA_ERR_TIMEOUT", 7: "FA_ERR_WORKSPACE_LIMIT"}
-EXPORTED = ("fa_fwd", "fa_fwd_mma", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_combine",
+EXPORTED = ("fa_fwd", "fa_fwd_host", "fa_fwd_mma", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_combine",
             "fa_fwd_splitkv_noalloc", "fa_fwd_fp8", "fa_fwd_blocksparse", "fa_bwd", "fa_bwd_workspace_bytes", "fa_get_device_status",
             "fa_status_string", "fa_version")
 
@@ -47,6 +47,8 @@ def lib():
             L.fa_fwd.restype = ctypes.c_int
             L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
                                  ctypes.c_int, vp]
+            L.fa_fwd_host.restype = ctypes.c_int
+            L.fa_fwd_host.argtypes = [vp] * 10 + [i64, i64, i64, i64, ctypes.c_float, ctypes.c_int, i64, vp]
             L.fa_fwd_mma.restype = ctypes.c_int
             L.fa_fwd_mma.argtypes = L.fa_fwd.argtypes
             L.fa_fwd_splitkv.restype = ctypes.c_int
@@ -81,6 +83,13 @@ def lib():
 def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
     """Raw call: pointers as ints, ``stream`` a cudaStream_t as int (0 = legacy default)."""
     return lib().fa_fwd(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), int(causal), stream)
+
+
+def fa_fwd_host(q, k, v, o, lse, q_dev, k_dev, v_dev, o_dev, lse_dev, B, H, N, d, scale, causal, n_groups,
+                stream) -> int:
+    """Raw call of the forward on host buffers (q..lse host, *_dev device staging)."""
+    return lib().fa_fwd_host(q, k, v, o, lse, q_dev, k_dev, v_dev, o_dev, lse_dev, B, H, N, d,
+                             ctypes.c_float(scale), int(causal), n_groups, stream)
 
 
 def fa_fwd_mma(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
@@ -186,6 +195,55 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | No
                     B, H, N, d, float(scale), bool(causal), s.cuda_stream)
     if st != FA_OK:
         raise FAError(st, "fa_fwd" if kernel == "tc" else "fa_fwd_mma")
+    return out, lse
+
+
+def host_staging(shape, device):
+    """Device staging buffers for ``forward_host``: (q, k, v, o) bf16 and lse fp32."""
+    B, H, N, d = shape
+    t = [torch.empty(shape, dtype=torch.bfloat16, device=device) for _ in range(4)]
+    return (*t, torch.empty((B, H, N), dtype=torch.float32, device=device))
+
+
+def forward_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
+                 causal: bool = False, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                 staging=None, n_groups: int = 0, device=None, stream: torch.cuda.Stream | None = None):
+    """O, LSE = attention(q, k, v) for HOST (CPU) tensors through ``fa_fwd_host``:
+    copies in, forward and copies out pipelined over groups of (b, h) slices.
+
+    q, k, v: contiguous bf16 CPU tensors [B, H, N, d] (pinned for full copy
+    speed).  ``staging`` is the tuple of device buffers from ``host_staging``
+    (allocated on ``device``, default the current CUDA device, when not given).
+    Returns host (O, LSE); the call is asynchronous on ``stream``: synchronise
+    it before reading them.
+    """
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must all be [B, H, N, d]")
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous bf16 CPU tensors")
+    B, H, N, d = q.shape
+    scale = default_scale(d) if scale is None else scale
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if staging is None:
+        staging = host_staging(q.shape, dev)
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=pin)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or out.is_cuda or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 CPU tensor shaped like q")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or lse.is_cuda or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 CPU tensor [B, H, N]")
+    qd, kd, vd, od, ld = staging
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        st = fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                         qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(), ld.data_ptr(),
+                         B, H, N, d, float(scale), bool(causal), int(n_groups), s.cuda_stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_host")
     return out, lse
 
 

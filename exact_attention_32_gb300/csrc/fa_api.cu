@@ -60,6 +60,18 @@ int check_pointer(const void *p, int dev)
     return FA_OK;
 }
 
+// A host pointer the copies may read or write: pinned or pageable host memory.
+int check_host_pointer(const void *p)
+{
+    if (p == nullptr) return FA_ERR_INVALID_ARG;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_INVALID_ARG;
+    }
+    return (a.type == cudaMemoryTypeHost || a.type == cudaMemoryTypeUnregistered) ? FA_OK : FA_ERR_INVALID_ARG;
+}
+
 bool overlaps(const void *a, uint64_t na, const void *b, uint64_t nb)
 {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -142,6 +154,60 @@ extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, floa
                       int64_t H, int64_t N, int64_t d, float scale, int causal, void *stream)
 {
     return validate_and_launch(fa_launch_tc, q, k, v, o, lse, B, H, N, d, scale, causal, stream);
+}
+
+extern "C" int fa_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse, void *q_dev,
+                           void *k_dev, void *v_dev, void *o_dev, float *lse_dev, int64_t B, int64_t H, int64_t N,
+                           int64_t d, float scale, int causal, int64_t n_groups, void *stream)
+{
+    int st = check_sizes(B, H, N, d);
+    if (st != FA_OK) return st;
+    if ((causal != 0 && causal != 1) || !(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+    const int64_t BH = B * H;
+    if (n_groups == 0) n_groups = BH < 4 ? BH : 4;
+    if (n_groups < 1 || n_groups > BH || n_groups > 64) return FA_ERR_INVALID_ARG;
+
+    int dev = 0, sm_count = 0;
+    if ((st = current_device(&dev, &sm_count)) != FA_OK) return st;
+    const void *dptrs[5] = {q_dev, k_dev, v_dev, o_dev, lse_dev};
+    for (const void *p : dptrs)
+        if ((st = check_pointer(p, dev)) != FA_OK) return st;
+    const void *hptrs[5] = {q, k, v, o, lse};
+    for (const void *p : hptrs)
+        if ((st = check_host_pointer(p)) != FA_OK) return st;
+    // outputs may overlap nothing; the device staging buffers may not overlap one another
+    const uint64_t tbytes = static_cast<uint64_t>(BH * N * d) * 2u;
+    const uint64_t lbytes = static_cast<uint64_t>(BH * N) * 4u;
+    if (overlaps(o, tbytes, lse, lbytes)) return FA_ERR_INVALID_ARG;
+    for (const void *in : {q, k, v})
+        if (overlaps(o, tbytes, in, tbytes) || overlaps(lse, lbytes, in, tbytes)) return FA_ERR_INVALID_ARG;
+    const void *dev_t[4] = {q_dev, k_dev, v_dev, o_dev};
+    for (int i = 0; i < 4; ++i) {
+        for (int j = i + 1; j < 4; ++j)
+            if (overlaps(dev_t[i], tbytes, dev_t[j], tbytes)) return FA_ERR_INVALID_ARG;
+        if (overlaps(dev_t[i], tbytes, lse_dev, lbytes)) return FA_ERR_INVALID_ARG;
+    }
+
+    FaHostProblem p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.lse = lse;
+    p.q_dev = q_dev;
+    p.k_dev = k_dev;
+    p.v_dev = v_dev;
+    p.o_dev = o_dev;
+    p.lse_dev = lse_dev;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.d = static_cast<int>(d);
+    p.scale = scale;
+    p.causal = causal;
+    p.n_groups = static_cast<int>(n_groups);
+    p.sm_count = sm_count;
+    return fa_run_host_pipeline(p, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fa_fwd_mma(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,

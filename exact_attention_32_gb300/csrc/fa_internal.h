@@ -53,3 +53,23 @@ int fa_bwd_take_status(cudaStream_t stream);
 
 // Warp-level tensor-core (mma.sync) kernel: one CTA per 128-row query tile.
 cudaError_t fa_launch_mma(const FaProblem &p, cudaStream_t stream);
+
+// Forward on host buffers (fa_fwd_host): q, k, v, o, lse are host pointers,
+// *_dev the caller's device staging buffers of the same shapes; the (b, h)
+// slices go in n_groups consecutive groups whose copies in, forward and
+// copies out are pipelined across two internal copy streams and `stream`.
+struct FaHostProblem {
+    const void *q, *k, *v;
+    void *o;
+    float *lse;
+    void *q_dev, *k_dev, *v_dev, *o_dev;
+    float *lse_dev;
+    int64_t B, H, N;
+    int d;
+    float scale;
+    int causal;
+    int n_groups;
+    int sm_count;
+};
+// Enqueue the pipeline; returns an fa_status.
+int fa_run_host_pipeline(const FaHostProblem &p, cudaStream_t stream);

@@ -79,6 +79,44 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            void *stream);
 
 /*
+ * fa_fwd_host - fa_fwd on HOST buffers: copies Q, K, V to the device, runs
+ * the forward, and copies O and LSE back, overlapping the copies with the
+ * compute.  The pages move tiles between HBM and on-chip memory
+ * ("FlashAttention: optimize data movement before counting FLOPs", section
+ * 02) and never discuss host memory; this entry point is this library's own.
+ * It is the end-to-end path, for callers whose data lives in host memory.
+ *
+ *   q, k, v : host, const bf16 [B, H, N, d] as in fa_fwd.  Pinned memory
+ *             (cudaHostAlloc, cudaHostRegister) copies at full speed;
+ *             pageable memory works but is staged by the driver.
+ *   o, lse  : host outputs, layouts as in fa_fwd; they must not overlap
+ *             q, k, v or each other.
+ *   q_dev, k_dev, v_dev, o_dev, lse_dev :
+ *             device staging buffers of the same shapes, owned by the caller,
+ *             16-byte aligned, on the current device, mutually disjoint.  On
+ *             return from a completed call they hold the inputs and outputs.
+ *   n_groups: the B*H (b, h) slices are processed in n_groups consecutive
+ *             groups of near-equal size (1 <= n_groups <= min(B*H, 64); 0
+ *             selects min(B*H, 4)).  Group g+1's copies in overlap group g's
+ *             forward, and group g's copies out overlap group g+1's forward.
+ *   stream  : the copies in start after the work already queued on `stream`;
+ *             work queued on `stream` afterwards starts after the last copy
+ *             out.  The call returns after enqueueing: synchronise `stream`
+ *             before reading o and lse on the host.
+ *
+ * The other arguments, and the results (bit for bit those of fa_fwd on the
+ * same device buffers), are as for fa_fwd.  The copies and the forward run on
+ * the caller's stream and two library-owned non-blocking streams, ordered by
+ * events.  Calls on one device serialise their enqueueing.  Returns FA_OK or
+ * an fa_status code.  Errors found before anything is enqueued leave
+ * everything untouched; FA_ERR_LAUNCH means a CUDA call failed part way.
+ */
+int fa_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                void *q_dev, void *k_dev, void *v_dev, void *o_dev, float *lse_dev,
+                int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
+                int64_t n_groups, void *stream);
+
+/*
  * fa_fwd_mma - the same operation, arguments, layouts and errors as fa_fwd,
  * computed by a warp-level tensor-core kernel (mma.sync m16n8k16, one CTA per
  * 128 query rows, cp.async double buffering) instead of the tcgen05 kernel.

@@ -75,3 +75,22 @@ def test_python_binding_exposes_the_abi():
     assert set(EXPORTED) == set(declared_functions())
     for name in EXPORTED:
         assert callable(getattr(fa, name))
+
+
+def _call_host(libfa, B=1, H=2, N=128, d=64, scale=0.125, causal=0, n_groups=0, ptr=16):
+    f = libfa.fa_fwd_host
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    f.argtypes = [vp] * 10 + [i64, i64, i64, i64, ctypes.c_float, ctypes.c_int, i64, vp]
+    f.restype = ctypes.c_int
+    return f(*([ptr] * 10), B, H, N, d, scale, causal, n_groups, None)
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(N=0), dict(scale=0.0), dict(scale=float("nan")), dict(causal=3),
+                                dict(n_groups=-1), dict(n_groups=3), dict(B=40, H=2, n_groups=65)])
+def test_host_entry_rejects_bad_arguments_before_any_device_call(libfa, kw):
+    # n_groups must lie in [1, min(B*H, 64)] (0 = default); B*H = 2 unless given
+    assert _call_host(libfa, **kw) == 1  # FA_ERR_INVALID_ARG
+
+
+def test_host_entry_unsupported_head_dim(libfa):
+    assert _call_host(libfa, d=96) == 2  # FA_ERR_UNSUPPORTED
