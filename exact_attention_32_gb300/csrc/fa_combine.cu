@@ -14,9 +14,13 @@
 // Memory-bound: one warp per row, lane s holds LSE_s (S <= 32 parts), each
 // lane owns d/32 consecutive output columns, read as one 16- or 8-byte vector
 // per part (a warp reads a 256- or 512-byte contiguous row), written as bf16.
+// The O vectors of up to 8 parts are loaded together, the first 8 alongside
+// the LSE load, so a row costs about one memory latency instead of two.
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 #include "fa_internal.h"
 
@@ -30,11 +34,19 @@ fa_combine_kernel(const float *__restrict__ o_parts, const float *__restrict__ l
                   __nv_bfloat16 *__restrict__ o, float *__restrict__ lse)
 {
     constexpr int PER = D / 32;  // output columns per lane
+    constexpr int kBatch = 8;    // parts whose O vectors are in flight together
+    using Vec = typename std::conditional<PER == 4, float4, float2>::type;
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     for (int64_t r = warp0; r < rows; r += n_warps) {
+        // the O vectors of the first parts do not depend on the weights: their
+        // loads go out together with the LSE load, before the reductions
         const float ls = lane < S ? lse_parts[lane * rows + r] : -INFINITY;
+        Vec x[kBatch];
+#pragma unroll
+        for (int s = 0; s < kBatch; ++s)
+            if (s < S) x[s] = *reinterpret_cast<const Vec *>(o_parts + (static_cast<int64_t>(s) * rows + r) * D + lane * PER);
         float m = ls;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -46,20 +58,28 @@ fa_combine_kernel(const float *__restrict__ o_parts, const float *__restrict__ l
         float acc[PER];
 #pragma unroll
         for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-#pragma unroll 4
-        for (int s = 0; s < S; ++s) {
-            const float ws = __shfl_sync(0xffffffffu, w, s) * inv_z;
-            const float *src = o_parts + (static_cast<int64_t>(s) * rows + r) * D + lane * PER;
-            if constexpr (PER == 4) {
-                const float4 x = *reinterpret_cast<const float4 *>(src);
-                acc[0] = fmaf(ws, x.x, acc[0]);
-                acc[1] = fmaf(ws, x.y, acc[1]);
-                acc[2] = fmaf(ws, x.z, acc[2]);
-                acc[3] = fmaf(ws, x.w, acc[3]);
-            } else {
-                const float2 x = *reinterpret_cast<const float2 *>(src);
-                acc[0] = fmaf(ws, x.x, acc[0]);
-                acc[1] = fmaf(ws, x.y, acc[1]);
+        for (int s0 = 0; s0 < S; s0 += kBatch) {
+            if (s0 > 0) {
+#pragma unroll
+                for (int s = 0; s < kBatch; ++s)
+                    if (s0 + s < S)
+                        x[s] = *reinterpret_cast<const Vec *>(o_parts + (static_cast<int64_t>(s0 + s) * rows + r) * D +
+                                                              lane * PER);
+            }
+#pragma unroll
+            for (int s = 0; s < kBatch; ++s) {
+                const float ws = __shfl_sync(0xffffffffu, w, (s0 + s) & 31) * inv_z;
+                if (s0 + s < S) {
+                    if constexpr (PER == 4) {
+                        acc[0] = fmaf(ws, x[s].x, acc[0]);
+                        acc[1] = fmaf(ws, x[s].y, acc[1]);
+                        acc[2] = fmaf(ws, x[s].z, acc[2]);
+                        acc[3] = fmaf(ws, x[s].w, acc[3]);
+                    } else {
+                        acc[0] = fmaf(ws, x[s].x, acc[0]);
+                        acc[1] = fmaf(ws, x[s].y, acc[1]);
+                    }
+                }
             }
         }
         __nv_bfloat16 *dst = o + r * D + lane * PER;
