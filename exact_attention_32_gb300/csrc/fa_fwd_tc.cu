@@ -85,6 +85,7 @@ struct Cfg {
     // barriers: q_full, q_empty, s_full[2], p_full[2], o_full[2], mma_done, kv_full[S], kv_empty[S]
     static constexpr int kNumBars = 9 + 2 * kStages;
     static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
+    static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
 };
 
 // Shared-memory addresses of the mbarriers, laid out from `base`: q_full,
