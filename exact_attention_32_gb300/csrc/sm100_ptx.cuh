@@ -425,12 +425,14 @@ __device__ __forceinline__ float add_bf16x2(float acc, uint32_t p)
 // v0 in the lowest byte.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float v0, float v1, float v2, float v3)
 {
-    uint32_t lo, hi;
-    asm("{\n.reg .b16 t;\ncvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\ncvt.u32.u16 %0, t;\n}\n"
-        : "=r"(lo) : "f"(v0), "f"(v1));
-    asm("{\n.reg .b16 t;\ncvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\ncvt.u32.u16 %0, t;\n}\n"
-        : "=r"(hi) : "f"(v2), "f"(v3));
-    return lo | (hi << 16);
+    uint32_t r;
+    asm("{\n.reg .b16 t0, t1;\n"
+        "cvt.rn.satfinite.e4m3x2.f32 t0, %2, %1;\n"
+        "cvt.rn.satfinite.e4m3x2.f32 t1, %4, %3;\n"
+        "mov.b32 %0, {t0, t1};\n}\n"
+        : "=r"(r)
+        : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+    return r;
 }
 
 // acc + the four E4M3 values of a packed word, in fp32 (decoded exactly through f16).
