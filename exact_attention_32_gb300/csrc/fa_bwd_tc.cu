@@ -553,7 +553,7 @@ cudaError_t launch_main(const FaBwdProblem &p, float *lse2, float *dvec, float *
         !make_map(&mdo, p.dout, BH, p.N, D))
         return cudaErrorInvalidValue;
     auto kern = fa_bwd_tc_kernel<D, CAUSAL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    cudaError_t e = set_max_dynamic_smem<fa_bwd_tc_kernel<D, CAUSAL>>(C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t n_blocks = (p.N + kBlock - 1) / kBlock;
     const int64_t grid = n_blocks * BH;

@@ -276,7 +276,7 @@ cudaError_t launch(const FaProblem &p, cudaStream_t stream)
 {
     const int smem = (kBr + 4 * kBc) * D * 2;
     auto kern = fa_fwd_mma_kernel<D, CAUSAL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = set_max_dynamic_smem<fa_fwd_mma_kernel<D, CAUSAL>>(smem);
     if (e != cudaSuccess) return e;
     const int n_qtiles = static_cast<int>((p.N + kBr - 1) / kBr);
     const int64_t BH = p.B * p.H;

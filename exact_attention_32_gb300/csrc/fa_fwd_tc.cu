@@ -685,7 +685,7 @@ cudaError_t launch(const FaProblem &p, void *o, float *lse, int n_splits, int kv
         !make_map(&mv, p.v, BH, p.N, D, C::kElem))
         return cudaErrorInvalidValue;
     auto kern = fa_fwd_tc_kernel<D, CAUSAL, OUT_F32, FP8, SPARSE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    cudaError_t e = set_max_dynamic_smem<fa_fwd_tc_kernel<D, CAUSAL, OUT_F32, FP8, SPARSE>>(C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t n_mblocks = (p.N + kQTiles * kBlockM - 1) / (kQTiles * kBlockM);
     const int64_t n_units = n_mblocks * BH * n_splits;

@@ -4,6 +4,23 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
+// cudaFuncSetAttribute(Kernel, MaxDynamicSharedMemorySize, bytes), made once per
+// kernel and device (bit d of `done` records device d) instead of on every launch.
+template <auto Kernel>
+cudaError_t set_max_dynamic_smem(int bytes)
+{
+    static std::atomic<uint64_t> done{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
 // One validated forward problem: contiguous [B, H, N, d] bf16 tensors.
 struct FaProblem {
     const void *q, *k, *v;
