@@ -84,7 +84,9 @@ struct Cfg {
     static constexpr int kBarOffset = (kQTiles + kStages) * kTileBytes;
     // barriers: q_full, q_empty, s_full[2], p_full[2], o_full[2], mma_done, kv_full[S], kv_empty[S]
     static constexpr int kNumBars = 9 + 2 * kStages;
-    static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
+    // block-sparse tile records: one per K/V ring slot, one per query tile
+    static constexpr int kMetaOffset = kBarOffset + kNumBars * 8 + 16;
+    static constexpr int kSmemBytes = 1024 + kMetaOffset + (kStages + 2) * 4;
     static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
 };
 
@@ -143,6 +145,37 @@ __device__ __forceinline__ uint32_t mask_word(const uint8_t *__restrict__ bm, in
     return last >= 31 ? m : (m & ((2u << last) - 1u));
 }
 
+// mask_word's bits for rows qa (.x) and qb (.y) separately, the 64 loads again
+// all in flight at once.
+__device__ __forceinline__ uint2 mask_row_words(const uint8_t *__restrict__ bm, int nb, int qa, int qb, int j0, int c,
+                                                int n)
+{
+    const int last = n - 1 - c;
+    const uint8_t *ra = bm + static_cast<int64_t>(qa) * nb + j0 + c;
+    const uint8_t *rb = bm + static_cast<int64_t>(qb) * nb + j0 + c;
+    uint32_t va[32], vb[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int k = i < last ? i : last;
+        va[i] = __ldg(ra + k);
+        vb[i] = __ldg(rb + k);
+    }
+    uint32_t ma = 0, mb = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        ma |= (va[i] != 0u ? 1u : 0u) << i;
+        mb |= (vb[i] != 0u ? 1u : 0u) << i;
+    }
+    const uint32_t keep = last >= 31 ? ~0u : ((2u << last) - 1u);
+    return make_uint2(ma & keep, mb & keep);
+}
+
+// Block-sparse tile record, published by the producer for every live K/V tile
+// (per K ring slot) and forwarded by the MMA thread with every S tile: the
+// tile index (bits 0-23), admitted by query tile 0 / 1 (bits 30 / 29), last
+// live tile of the unit (bit 31).
+constexpr uint32_t kMetaTile = 0xffffffu, kMetaOwn0 = 1u << 30, kMetaOwn1 = 1u << 29, kMetaLast = 1u << 31;
+
 __device__ __forceinline__ int unit_index(int r)
 {
     const int G = gridDim.x, c = blockIdx.x;
@@ -192,13 +225,15 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const uint32_t sRing = s_base + kQTiles * C::kTileBytes;
     const uint32_t bar0 = s_base + C::kBarOffset;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kBarOffset + C::kNumBars * 8);
+    volatile uint32_t *kv_meta = reinterpret_cast<volatile uint32_t *>(smem + C::kMetaOffset);  // [kStages]
+    volatile uint32_t *s_meta = kv_meta + C::kStages;                                            // [kQTiles]
 
     const Bars<C::kStages> bars{bar0};
     // K/V tiles a unit processes: all of its range, or in block-sparse mode those
-    // the mask admits for either query block of the unit.  In the tile loops,
-    // `word` holds the live bits of the 32-tile group of j (loaded at each group
-    // start) and j jumps to the group's next live tile, or past the group when
-    // none is left, so dead tiles cost no loop iterations.
+    // the mask admits for either query block of the unit.  The producer finds
+    // them (32 tiles per mask read) and publishes a record per live tile, which
+    // the MMA thread and the softmax warps follow; any_live (the same mask rows)
+    // tells every role which units have no live tile at all.
     auto unit_word = [&](const Unit &w, int c) {
         const int qa = w.q_row0 / kBlockM, qb = qa + 1 < nb ? qa + 1 : qa;
         return mask_word(bm, nb, qa, qb, w.j0, c, w.n_kv);
@@ -220,7 +255,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         mbar_init(bars.q_full(), 1);
         mbar_init(bars.q_empty(), 1);
         for (int t = 0; t < 2; ++t) {
-            mbar_init(bars.s_full(t), 1);
+            // block-sparse: the commit and an arrive of the MMA thread that publishes s_meta[t]
+            mbar_init(bars.s_full(t), SPARSE ? 2 : 1);
             mbar_init(bars.p_full(t), kBlockM / 32);  // one arrive per softmax warp
             mbar_init(bars.o_full(t), 1);
         }
@@ -264,16 +300,36 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &tm_q, bars.q_full(), a * (128 / C::kElem),
                                     w.q_row0 + t * kBlockM, w.bh);
                 ++uc;
-                uint32_t word = 0;
-                for (int j = 0; j < w.n_kv && ok; ++j) {
-                    if constexpr (SPARSE) {
-                        if ((j & 31) == 0) word = unit_word(w, j);
-                        const uint32_t rest = word >> (j & 31);
-                        if (rest == 0) {
-                            j |= 31;
-                            continue;
+                // block-sparse: the live tiles in order, each published in its K slot's record
+                // with its admission bits and a last-tile flag (found by looking one live
+                // tile ahead); wa / wb are the admission bits of the two query blocks for the
+                // 32-tile group `grp`
+                uint32_t wa = 0, wb = 0;
+                int grp = -1;
+                auto next_live = [&](int from) {  // the first live tile >= from, or -1
+                    for (int c = from & ~31; c < w.n_kv; c += 32) {
+                        if ((c >> 5) != grp) {
+                            const int qa = w.q_row0 / kBlockM;
+                            const uint2 wab = mask_row_words(bm, nb, qa, qa + 1 < nb ? qa + 1 : qa, w.j0, c, w.n_kv);
+                            wa = wab.x;
+                            wb = qa + 1 < nb ? wab.y : 0u;  // a second query block past the last row admits nothing
+                            grp = c >> 5;
                         }
-                        j += __ffs(rest) - 1;
+                        const uint32_t rest = (from > c) ? ((wa | wb) >> (from - c)) << (from - c) : (wa | wb);
+                        if (rest != 0) return c + __ffs(rest) - 1;
+                    }
+                    return -1;
+                };
+                int j_live = SPARSE ? next_live(0) : 0;
+                for (int j = 0; j < w.n_kv && ok; ++j) {
+                    uint32_t meta = 0;
+                    if constexpr (SPARSE) {
+                        if (j_live < 0) break;
+                        j = j_live;
+                        const uint32_t bit = 1u << (j & 31);
+                        meta = static_cast<uint32_t>(j) | ((wa & bit) ? kMetaOwn0 : 0u) | ((wb & bit) ? kMetaOwn1 : 0u);
+                        j_live = next_live(j + 1);
+                        if (j_live < 0) meta |= kMetaLast;
                     }
                     for (int kind = 0; kind < 2; ++kind, ++it) {
                         const int slot = it % C::kStages, use = it / C::kStages;
@@ -281,6 +337,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             ok = false;
                             break;
                         }
+                        if (SPARSE && kind == 0) kv_meta[slot] = meta;  // released by the arrive below
                         mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
                         const CUtensorMap *tm = kind == 0 ? &tm_k : &tm_v;
                         for (int a = 0; a < C::kAtoms; ++a)
@@ -321,23 +378,15 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 uint32_t prev_v_lo = 0;
                 int prev_v = -1;
                 int jj = 0;  // K/V tiles of this unit processed so far
-                uint32_t word = 0;
+                // (block-sparse: the producer's records give the live tiles; j only counts)
                 for (int j = 0; j < w.n_kv && ok; ++j) {
-                    if constexpr (SPARSE) {
-                        if ((j & 31) == 0) word = unit_word(w, j);
-                        const uint32_t rest = word >> (j & 31);
-                        if (rest == 0) {
-                            j |= 31;
-                            continue;
-                        }
-                        j += __ffs(rest) - 1;
-                    }
                     const int kslot = it % C::kStages, kuse = it / C::kStages;
                     ++it;
                     const int vslot = it % C::kStages, vuse = it / C::kStages;
                     ++it;
                     if (!(ok = mbar_wait(bars.full(kslot), kuse & 1, kWaitLimitNs))) break;
                     tc_fence_after();
+                    const uint32_t meta = SPARSE ? kv_meta[kslot] : 0u;
                     const uint32_t dk_lo = static_cast<uint32_t>(dk0) + kslot * kTile16;
                     for (int t = 0; t < kQTiles && ok; ++t) {
                         if (jj > 0) {
@@ -354,6 +403,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                                 dv_hi, idO, (jj > 1 || kk > 0) ? 1u : 0u);
                             }
                         }
+                        if constexpr (SPARSE)  // this S tile's record, for the softmax (published by the arrive below)
+                            s_meta[t] = (meta & (kMetaTile | kMetaLast)) | (((meta >> (30 - t)) & 1u) << 30);
                         const uint32_t aq_lo = dq_lo + t * kTile16;
 #pragma unroll
                         for (int kk = 0; kk < C::kSSteps; ++kk) {
@@ -366,6 +417,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                             kk > 0 ? 1u : 0u);
                         }
                         mma_commit(bars.s_full(t));
+                        if constexpr (SPARSE) mbar_arrive(bars.s_full(t));
                     }
                     if (!ok) break;
                     mma_commit(bars.empty(kslot));
@@ -376,6 +428,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     prev_v_lo = static_cast<uint32_t>(dv0) + vslot * kTile16;
                     ++jg;
                     ++jj;
+                    if (SPARSE && (meta & kMetaLast) != 0u) break;
                 }
                 if (!ok) break;
                 mma_commit(bars.q_empty());  // the last reads of this unit's Q are issued
@@ -416,16 +469,14 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int row_g = w.q_row0 + t * kBlockM + row;
             const int64_t out_row = (static_cast<int64_t>(w.split) * BH + w.bh) * N + row_g;
             const bool qb_ok = !SPARSE || (w.q_row0 / kBlockM + t < nb);
-            // block-sparse: tiles j .. j+31 of the unit, one lane per tile.  Returns the
-            // tiles either query block admits; own_r gets those this warpgroup's block admits.
-            uint32_t own_r = 0;
+            // block-sparse: the tiles j .. j+31 of the unit that either query block admits
+            // (one lane per tile), to find units with no admitted tile
             auto load_words = [&](int j) -> uint32_t {
                 const int qa = w.q_row0 / kBlockM, qb2 = qa + 1 < nb ? qa + 1 : qa;
                 const bool in = j + lane < w.n_kv;
                 const int64_t kj = w.j0 + j + lane;
                 const uint8_t a = in ? __ldg(bm + qa * static_cast<int64_t>(nb) + kj) : 0;
                 const uint8_t b = in ? __ldg(bm + qb2 * static_cast<int64_t>(nb) + kj) : 0;
-                own_r = __ballot_sync(0xffffffffu, qb_ok && (t == 0 ? a : b) != 0);
                 return __ballot_sync(0xffffffffu, (a | b) != 0);
             };
             bool unit_live = w.n_kv > 0;
@@ -456,19 +507,16 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             float l = 0.f;            // exp-sum relative to m_ref (fp32 terms; gives LSE)
             float lr = 0.f;           // the same sum over the bf16-rounded terms the MMA sees (normalises O)
             int jj = 0;  // K/V tiles of this unit processed so far
-            uint32_t word = 0;  // block-sparse: live tiles of the 32-tile group of j
-            for (int j = 0; j < w.n_kv; ++j) {
-                // block-sparse: dead tiles are stepped over one by one here (moving j
-                // inside this loop, as the producer and MMA loops do, costs spills)
-                if constexpr (SPARSE) {
-                    if ((j & 31) == 0) word = load_words(j);
-                    if (((word >> (j & 31)) & 1u) == 0) continue;
-                }
+            // block-sparse: the loop counts the unit's live tiles; each one's index and
+            // admission bit come with its S tile (the MMA thread's record)
+            for (int jc = 0; jc < w.n_kv; ++jc) {
                 if (!mbar_wait_warp(bars.s_full(t), jg & 1, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                const uint32_t meta = SPARSE ? s_meta[t] : 0u;
+                const int j = SPARSE ? static_cast<int>(meta & kMetaTile) : jc;
                 float s[kBlockN];
                 {
                     uint32_t r[4][32];
@@ -481,7 +529,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
                 }
                 const int k0 = (w.j0 + j) * kBlockN;
-                if (SPARSE && (!qb_ok || ((own_r >> (j & 31)) & 1u) == 0)) {
+                if (SPARSE && (!qb_ok || (meta & kMetaOwn0) == 0u)) {
 #pragma unroll
                     for (int i = 0; i < kBlockN; ++i) s[i] = -INFINITY;  // block not admitted for this query tile
                 }
@@ -584,6 +632,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (lane == 0) mbar_arrive(bars.p_full(t));
                 ++jg;
                 ++jj;
+                if (SPARSE && (meta & kMetaLast) != 0u) break;
             }
             if (!ok || !(ok = mbar_wait_warp(bars.o_full(t), uc & 1, kWaitLimitNs))) break;
             tc_fence_after();
