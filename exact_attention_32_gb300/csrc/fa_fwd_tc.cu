@@ -182,11 +182,26 @@ __device__ __forceinline__ int unit_index(int r)
     return r * G + ((r & 1) ? (G - 1 - c) : c);
 }
 
-template <bool CAUSAL>
+// SPLIT: the launch covers key splits (the split-KV partials); otherwise every
+// item spans all N keys, and the split fields are compile-time constants, so
+// the single-split variants carry none of the key-range arithmetic.
+template <bool CAUSAL, bool SPLIT>
 __device__ __forceinline__ Unit unit_of(int u, int N, int BH, int n_mblocks, int n_splits, int kv_chunk)
 {
-    const int rb = u / n_splits;  // row-block unit
     Unit w;
+    if constexpr (!SPLIT) {
+        const int mb = CAUSAL ? (n_mblocks - 1 - u / BH) : (u / BH);
+        w.bh = u % BH;
+        w.q_row0 = mb * (kQTiles * kBlockM);
+        w.split = 0;
+        w.kv_begin = 0;
+        w.kv_end = N;
+        w.j0 = 0;
+        const int k_hi = CAUSAL ? min(N, w.q_row0 + kQTiles * kBlockM) : N;
+        w.n_kv = (k_hi + kBlockN - 1) / kBlockN;
+        return w;
+    }
+    const int rb = u / n_splits;  // row-block unit
     w.split = u - rb * n_splits;
     const int mb = CAUSAL ? (n_mblocks - 1 - rb / BH) : (rb / BH);
     w.bh = rb % BH;
@@ -287,7 +302,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             bool ok = true;
             int it = 0, uc = 0;
             for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
-                const Unit w = unit_of<CAUSAL>(u, N, BH, n_mblocks, n_splits, kv_chunk);
+                const Unit w = unit_of<CAUSAL, OUT_F32>(u, N, BH, n_mblocks, n_splits, kv_chunk);
                 if (!any_live(w)) continue;  // no admitted key: nothing to load
                 // the Q buffers are free once the previous unit's last S MMAs have completed
                 if (!mbar_wait(bars.q_empty(), (uc & 1) ^ 1, kWaitLimitNs)) {
@@ -371,7 +386,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             bool ok = true;
             int it = 0, uc = 0, jg = 0;  // ring position, units done, K/V tiles done (all units)
             for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
-                const Unit w = unit_of<CAUSAL>(u, N, BH, n_mblocks, n_splits, kv_chunk);
+                const Unit w = unit_of<CAUSAL, OUT_F32>(u, N, BH, n_mblocks, n_splits, kv_chunk);
                 if (!any_live(w)) continue;
                 if (!(ok = mbar_wait(bars.q_full(), uc & 1, kWaitLimitNs))) break;
                 tc_fence_after();
@@ -465,7 +480,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         bool ok = true;
         int jg = 0, uc = 0;
         for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
-            const Unit w = unit_of<CAUSAL>(u, N, BH, n_mblocks, n_splits, kv_chunk);
+            const Unit w = unit_of<CAUSAL, OUT_F32>(u, N, BH, n_mblocks, n_splits, kv_chunk);
             const int row_g = w.q_row0 + t * kBlockM + row;
             const int64_t out_row = (static_cast<int64_t>(w.split) * BH + w.bh) * N + row_g;
             const bool qb_ok = !SPARSE || (w.q_row0 / kBlockM + t < nb);
