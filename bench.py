@@ -452,8 +452,11 @@ def run_ours(args, rank, world, local):
     if st != 0:
         raise fa.FAError(st, "timed region")
     total_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
-    launch_ms = max_over_ranks(launch_ms, world)
+    durations = sorted(s.elapsed_time(e) for s, e in zip(starts, ends))
+    launch_ms = max_over_ranks(statistics.mean(durations), world)
+    # the distribution of this rank's per-launch times (nearest-rank percentiles)
+    pct = {f"p{q}": durations[min(len(durations) - 1, max(0, round(q / 100 * len(durations)) - 1))]
+           for q in (10, 50, 90)}
 
     if flush is not None:  # the timed region also holds the flushes: count the launches only
         total_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)), world)
@@ -518,6 +521,8 @@ def run_ours(args, rank, world, local):
                      "algorithmic_bytes_per_launch": w.min_bytes,
                      "launch_ms": launch_ms},
         "gpu_launches": K,
+        "launch_ms_percentiles": pct,
+        "max_memory_allocated_bytes": torch.cuda.max_memory_allocated(dev),
         "impl": "ours",
     }
     if e2e:
