@@ -428,3 +428,26 @@ def test_blocksparse_row_without_blocks():
     o, lse = oracle.attention_blocksparse(q, k, v, 0.5, False, mask)
     assert np.all(o[:, :, 128:] == 0) and np.all(np.isneginf(lse[:, :, 128:]))
     assert np.all(np.isfinite(lse[:, :, :128]))
+
+
+@pytest.mark.parametrize("name,head", [("b1_h1_n256_d64", (0, 0)), ("b16_h16_n1000_d64_causal_q8", (3, 7))])
+def test_dense_matches_library_softmax_at_workload_size(name, head):
+    # the textbook form with library routines: scores by a matrix product, a
+    # library softmax along the keys, then another matrix product, all fp64
+    from scipy.special import logsumexp, softmax
+
+    from exact_attention_32_gb300 import WORKLOADS, workload_inputs
+
+    w = WORKLOADS[name]
+    q, k, v = workload_inputs(w)
+    b, h = head
+    qs, ks, vs = (t[b:b + 1, h:h + 1].contiguous() for t in (q, k, v))
+    o, lse = oracle.attention(qs, ks, vs, w.scale, w.causal)
+    qd, kd, vd = (t[0, 0].double().numpy() for t in (qs, ks, vs))
+    s = float(np.float32(w.scale)) * (qd @ kd.T)
+    if w.causal:
+        s = np.where(np.tril(np.ones_like(s, dtype=bool)), s, -np.inf)
+    o_lib = softmax(s, axis=1) @ vd
+    lse_lib = logsumexp(s, axis=1)
+    assert np.allclose(o[0, 0], o_lib, rtol=1e-12, atol=1e-12)
+    assert np.allclose(lse[0, 0], lse_lib, rtol=1e-12, atol=1e-12)
