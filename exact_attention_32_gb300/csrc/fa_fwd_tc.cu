@@ -81,7 +81,13 @@ struct Cfg {
     static constexpr int kSSteps = kRowBytes / 32;          // S MMA K steps (32 bytes of each row)
     static constexpr int kPVKeys = FP8 ? 32 : 16;           // keys per P V MMA
     static constexpr int kPVSteps = kBlockN / kPVKeys;
-    static constexpr int kBarOffset = (kQTiles + kStages) * kTileBytes;
+    // d = 64 (bf16): the P V MMA runs at N = 80.  B's extra 16 columns come from a
+    // constant block (a column of ones, then zeros), so column 64 of O accumulates
+    // the row sum of exactly the bf16 P that the MMA multiplies, rescaled with O.
+    static constexpr bool kOnesCol = (D == 64 && !FP8);
+    static constexpr int kPVN = kOnesCol ? 80 : D;             // N of the P V MMA
+    static constexpr int kOnesOffset = (kQTiles + kStages) * kTileBytes;
+    static constexpr int kBarOffset = kOnesOffset + (kOnesCol ? kBlockN * 128 : 0);
     // barriers: q_full, q_empty, s_full[2], p_full[2], o_full[2], mma_done, kv_full[S], kv_empty[S]
     static constexpr int kNumBars = 9 + 2 * kStages;
     // block-sparse tile records: one per K/V ring slot, one per query tile
@@ -238,6 +244,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const uint32_t s_base = smem_u32(smem);
     const uint32_t sQ = s_base;  // kQTiles tiles
     const uint32_t sRing = s_base + kQTiles * C::kTileBytes;
+    const uint32_t sOnes = s_base + C::kOnesOffset;  // d = 64 only: B's columns 64..79 of the P V MMA
     const uint32_t bar0 = s_base + C::kBarOffset;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kBarOffset + C::kNumBars * 8);
     volatile uint32_t *kv_meta = reinterpret_cast<volatile uint32_t *>(smem + C::kMetaOffset);  // [kStages]
@@ -281,6 +288,16 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mbar_init(bars.empty(s), 1);
         }
         fence_mbar_init();
+    }
+    if constexpr (C::kOnesCol) {
+        // kBlockN key rows of 128 bytes in the 128-byte swizzle V uses: bf16 1.0 at
+        // column 0 of every row (16-byte chunk 0 lands at chunk r mod 8), zeros elsewhere
+        for (int i = threadIdx.x; i < kBlockN * 8; i += blockDim.x) {
+            const int r = i >> 3, c = i & 7;
+            reinterpret_cast<uint4 *>(smem + C::kOnesOffset)[i] =
+                make_uint4(c == (r & 7) ? 0x3F80u : 0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // visible to the tensor cores' reads
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), 512);
@@ -373,13 +390,14 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (lane == 0) {
             constexpr uint32_t idS = FP8 ? idesc_e4m3_f32(kBlockM, kBlockN, false)
                                          : idesc_bf16_f32(kBlockM, kBlockN, false);
-            constexpr uint32_t idO = FP8 ? idesc_e4m3_f32(kBlockM, D, true) : idesc_bf16_f32(kBlockM, D, true);
+            constexpr uint32_t idO =
+                FP8 ? idesc_e4m3_f32(kBlockM, D, true) : idesc_bf16_f32(kBlockM, C::kPVN, true);
             // descriptors are built once; a K step only moves the start address
             // (low 32 bits, in 16-byte units): +32 bytes inside a 128-byte-wide
             // column block, +16 KB to the next block (S), +2 KB per 16 keys (P V)
             const uint64_t dq = smem_desc_sw128(sQ, 16, 1024);
             const uint64_t dk0 = smem_desc_sw128(sRing, 16, 1024);
-            const uint64_t dv0 = smem_desc_sw128(sRing, kBlockN * 128, 1024);
+            const uint64_t dv0 = smem_desc_sw128(sRing, C::kOnesCol ? sOnes - sRing : kBlockN * 128, 1024);
             const uint32_t dq_lo = static_cast<uint32_t>(dq), dq_hi = static_cast<uint32_t>(dq >> 32);
             const uint32_t dk_hi = static_cast<uint32_t>(dk0 >> 32), dv_hi = static_cast<uint32_t>(dv0 >> 32);
             constexpr uint32_t kTile16 = C::kTileBytes >> 4;
@@ -440,7 +458,9 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     if (!(ok = mbar_wait(bars.full(vslot), vuse & 1, kWaitLimitNs))) break;
                     tc_fence_after();
                     prev_v = vslot;
-                    prev_v_lo = static_cast<uint32_t>(dv0) + vslot * kTile16;
+                    // d = 64: the block "after" V's 64 columns is the ones block, so the leading
+                    // byte offset (bits 16..29) falls by what the start address (bits 0..13) gains
+                    prev_v_lo = static_cast<uint32_t>(dv0) + vslot * (C::kOnesCol ? kTile16 - (kTile16 << 16) : kTile16);
                     ++jg;
                     ++jj;
                     if (SPARSE && (meta & kMetaLast) != 0u) break;
@@ -520,7 +540,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const float scale_u = FP8 ? scale * qs[w.bh] * ks[w.bh] : scale;
             float m_ref = -INFINITY;  // reference max, unscaled units
             float l = 0.f;            // exp-sum relative to m_ref (fp32 terms; gives LSE)
-            float lr = 0.f;           // the same sum over the bf16-rounded terms the MMA sees (normalises O)
+            float lr = 0.f;           // the same sum over the bf16-rounded terms the MMA sees (normalises O;
+                                      // d = 64: accumulated by the MMA in column 64 of O instead)
             int jj = 0;  // K/V tiles of this unit processed so far
             // block-sparse: the loop counts the unit's live tiles; each one's index and
             // admission bit come with its S tile (the MMA thread's record)
@@ -611,9 +632,11 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         for (int i = 0; i < 16; ++i) {
                             const float2 x = fma2(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), c2, nmc2);
                             const float p0 = ex2(x.x), p1 = ex2(x.y);
-                            lf[i & 3] = add2(lf[i & 3], make_float2(p0, p1));
+                            // one partial per chunk (d = 64: fewer live registers, no spills)
+                            const int pl = C::kOnesCol ? c : (i & 3);
+                            lf[pl] = add2(lf[pl], make_float2(p0, p1));
                             p[i] = pack_bf16x2(p0, p1);
-                            lq[i & 3] = add_bf16x2(lq[i & 3], p[i]);
+                            if constexpr (!C::kOnesCol) lq[i & 3] = add_bf16x2(lq[i & 3], p[i]);
                         }
                         tmem_st16(tS + c * 16, p);
                     }
@@ -621,7 +644,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const float2 lf01 = add2(lf[0], lf[1]), lf23 = add2(lf[2], lf[3]);
                 const float2 lfs = add2(lf01, lf23);
                 l = l * alpha + (lfs.x + lfs.y);
-                lr = lr * alpha + ((lq[0] + lq[1]) + (lq[2] + lq[3]));
+                if constexpr (!C::kOnesCol) lr = lr * alpha + ((lq[0] + lq[1]) + (lq[2] + lq[3]));
                 // numerator rescale u *= alpha (u holds P V up to the previous tile, complete:
                 // the commit that signalled this S was issued after that MMA); nothing to
                 // scale on the unit's first tile
@@ -639,6 +662,11 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             r[i + 1] = __float_as_uint(y.y);
                         }
                         tmem_st32(tO + c * 32, r);
+                    }
+                    if constexpr (C::kOnesCol) {  // the rounded row sum in column 64
+                        const float lc = __uint_as_float(tmem_ld1(tO + 64));
+                        tmem_wait_ld();
+                        tmem_st1(tO + 64, __float_as_uint(lc * alpha));
                     }
                 }
                 tmem_wait_st();
@@ -658,6 +686,10 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // error.  The next unit's first P V (which overwrites O_t) is issued
             // only after this warpgroup's next p_full arrive, so the reads here are safe.
             // a row with no admitted key in this split has l = 0: O = 0, LSE = -inf
+            if constexpr (C::kOnesCol) {
+                lr = __uint_as_float(tmem_ld1(tO + 64));
+                tmem_wait_ld();
+            }
             const float inv_l = lr > 0.f ? (FP8 ? vs[w.bh] : 1.f) / lr : 0.f;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
