@@ -66,6 +66,7 @@ constexpr int kThreads = 320;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr float kRescaleLog2 = 8.0f;            // rescale when the max grows by more than 2^8
+constexpr float kHeavyShare = 0.25f;            // bf16 P, d = 128: see "heavy" in the softmax
 constexpr uint64_t kWaitLimitNs = 1000000000ull;    // 1 s per pipeline wait
 constexpr uint64_t kCleanupLimitNs = 20000000ull;    // 20 ms per wait while winding down
 
@@ -502,7 +503,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
             const Unit w = unit_of<CAUSAL, OUT_F32>(u, N, BH, n_mblocks, n_splits, kv_chunk);
             const int row_g = w.q_row0 + t * kBlockM + row;
-            const int64_t out_row = (static_cast<int64_t>(w.split) * BH + w.bh) * N + row_g;
+            auto out_row_of = [&]() { return (static_cast<int64_t>(w.split) * BH + w.bh) * N + row_g; };
             const bool qb_ok = !SPARSE || (w.q_row0 / kBlockM + t < nb);
             // block-sparse: the tiles j .. j+31 of the unit that either query block admits
             // (one lane per tile), to find units with no admitted tile
@@ -522,6 +523,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (!unit_live) {
                 // no admitted key in this split (or block mask): O = 0, LSE = -inf (no weight when merged)
                 if (row_g < N) {
+                    const int64_t out_row = out_row_of();
                     if (OUT_F32) {
                         float4 *orow = reinterpret_cast<float4 *>(static_cast<float *>(o) + out_row * D);
 #pragma unroll
@@ -537,11 +539,9 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             // exponent constant and LSE scale of this slice (E4M3 scales folded in)
             const float c_u = FP8 ? scale_log2 * qs[w.bh] * ks[w.bh] : scale_log2;
-            const float scale_u = FP8 ? scale * qs[w.bh] * ks[w.bh] : scale;
             float m_ref = -INFINITY;  // reference max, unscaled units
             float l = 0.f;            // exp-sum relative to m_ref (fp32 terms; gives LSE)
-            float lr = 0.f;           // the same sum over the bf16-rounded terms the MMA sees (normalises O;
-                                      // d = 64: accumulated by the MMA in column 64 of O instead)
+            float lr = 0.f;           // the divisor of O (see the row sums below)
             int jj = 0;  // K/V tiles of this unit processed so far
             // block-sparse: the loop counts the unit's live tiles; each one's index and
             // admission bit come with its S tile (the MMA thread's record)
@@ -600,6 +600,13 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 // P = exp2(s * scale * log2 e - m_ref * scale * log2 e), bf16, over the first 64 columns
                 // of S_t; fp32 and bf16-rounded row sums in independent partial accumulators
                 const float mc = (m_ref == -INFINITY ? 0.f : m_ref) * c_u;
+                // how the divisor of O is summed for bf16 P at d = 128 (see the row sums below):
+                // every term inline in the key-split forward, else per tile as needed
+                constexpr bool kInlineSum = !FP8 && !C::kOnesCol && OUT_F32;
+                constexpr bool kHeavyTiles = !FP8 && !C::kOnesCol && !OUT_F32;
+                bool heavy = false;
+                if constexpr (kHeavyTiles)
+                    heavy = __any_sync(0xffffffffu, ex2(fmaf(mt, c_u, -mc)) > kHeavyShare * (l * alpha));
                 const float2 c2 = make_float2(c_u, c_u), nmc2 = make_float2(-mc, -mc);
                 float2 lf[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                 make_float2(0.f, 0.f)};
@@ -632,19 +639,50 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         for (int i = 0; i < 16; ++i) {
                             const float2 x = fma2(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), c2, nmc2);
                             const float p0 = ex2(x.x), p1 = ex2(x.y);
-                            // one partial per chunk (d = 64: fewer live registers, no spills)
-                            const int pl = C::kOnesCol ? c : (i & 3);
-                            lf[pl] = add2(lf[pl], make_float2(p0, p1));
                             p[i] = pack_bf16x2(p0, p1);
-                            if constexpr (!C::kOnesCol) lq[i & 3] = add_bf16x2(lq[i & 3], p[i]);
+                            if constexpr (kInlineSum) {
+                                lf[i & 3] = add2(lf[i & 3], make_float2(p0, p1));
+                                lq[i & 3] = add_bf16x2(lq[i & 3], p[i]);
+                            } else {
+                                lf[c] = add2(lf[c], make_float2(p0, p1));  // one partial per chunk
+                            }
                         }
                         tmem_st16(tS + c * 16, p);
                     }
                 }
                 const float2 lf01 = add2(lf[0], lf[1]), lf23 = add2(lf[2], lf[3]);
                 const float2 lfs = add2(lf01, lf23);
+                if constexpr (FP8 || kInlineSum) {
+                    lr = lr * alpha + ((lq[0] + lq[1]) + (lq[2] + lq[3]));
+                } else if constexpr (kHeavyTiles) {
+                    // d = 128: O is divided by lr, which must be the sum of the bf16 P the
+                    // MMA sees wherever few keys carry a row (a 2^-9 mismatch on a top
+                    // weight shows in O), while over many comparable keys the fp32 sum's
+                    // rounding differences average out.  So the exact rounded sum is
+                    // taken only in "heavy" tiles, where for some row of the warp the
+                    // tile's largest P exceeds kHeavyShare of the row's running sum
+                    // (always the unit's first tile): P is read back from tensor memory
+                    // and summed with mixed-precision adds.  Any key whose final weight
+                    // exceeds kHeavyShare lies in a heavy tile.  Light tiles add their fp32
+                    // sum.  (d = 64 gets the rounded sum from the MMA, column 64 of O; the
+                    // key-split forward, whose variants run out of registers with this
+                    // branch, sums every rounded term inline.)
+                    float add = lfs.x + lfs.y;
+                    if (heavy) {
+                        tmem_wait_st();
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t r[32];
+                            tmem_ld32(tS + h * 32, r);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) lq[i & 3] = add_bf16x2(lq[i & 3], r[i]);
+                        }
+                        add = (lq[0] + lq[1]) + (lq[2] + lq[3]);
+                    }
+                    lr = lr * alpha + add;
+                }
                 l = l * alpha + (lfs.x + lfs.y);
-                if constexpr (!C::kOnesCol) lr = lr * alpha + ((lq[0] + lq[1]) + (lq[2] + lq[3]));
                 // numerator rescale u *= alpha (u holds P V up to the previous tile, complete:
                 // the commit that signalled this S was issued after that MMA); nothing to
                 // scale on the unit's first tile
@@ -690,6 +728,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 lr = __uint_as_float(tmem_ld1(tO + 64));
                 tmem_wait_ld();
             }
+            const int64_t out_row = out_row_of();
             const float inv_l = lr > 0.f ? (FP8 ? vs[w.bh] : 1.f) / lr : 0.f;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -717,6 +756,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                 }
             }
+            const float scale_u = FP8 ? scale * qs[w.bh] * ks[w.bh] : scale;
             if (row_g < N) lse[out_row] = l > 0.f ? m_ref * scale_u + logf(l) : -INFINITY;
             ++uc;
         }

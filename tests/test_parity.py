@@ -93,6 +93,18 @@ def test_workload_sampled_rows(name, kernel):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("causal", [False, True])
+def test_large_logit_d128_every_row(causal, kernel):
+    # the large-logit recipe (Q x 8) at d = 128: many rows have one or two
+    # dominant keys, where the P rounding and the choice of the divisor of O show
+    q, k, v = make_inputs(16, 16, 1000, 128, seed=88 + causal, q_gain=8.0)
+    scale = float(np.float32(1 / np.sqrt(128)))
+    o, lse = run_gpu(q, k, v, scale, causal, kernel)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, causal)
+    check(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 def test_large_logit_rows_are_sharp(kernel):
     # Q x 8: logits reach about +-50; the result still matches where P is
     # nearly one-hot
