@@ -66,7 +66,7 @@ constexpr int kThreads = 320;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr float kRescaleLog2 = 8.0f;            // rescale when the max grows by more than 2^8
-constexpr float kHeavyShare = 0.25f;            // bf16 P, d = 128: see "heavy" in the softmax
+constexpr float kHeavyShare = 0.25f;            // d = 128: see "heavy" in the softmax
 constexpr uint64_t kWaitLimitNs = 1000000000ull;    // 1 s per pipeline wait
 constexpr uint64_t kCleanupLimitNs = 20000000ull;    // 20 ms per wait while winding down
 
@@ -600,10 +600,10 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 // P = exp2(s * scale * log2 e - m_ref * scale * log2 e), bf16, over the first 64 columns
                 // of S_t; fp32 and bf16-rounded row sums in independent partial accumulators
                 const float mc = (m_ref == -INFINITY ? 0.f : m_ref) * c_u;
-                // how the divisor of O is summed for bf16 P at d = 128 (see the row sums below):
-                // every term inline in the key-split forward, else per tile as needed
+                // how the divisor of O is summed at d = 128 (see the row sums below): every
+                // term inline in the key-split forward, else per tile as needed
                 constexpr bool kInlineSum = !FP8 && !C::kOnesCol && OUT_F32;
-                constexpr bool kHeavyTiles = !FP8 && !C::kOnesCol && !OUT_F32;
+                constexpr bool kHeavyTiles = !C::kOnesCol && !OUT_F32;
                 bool heavy = false;
                 if constexpr (kHeavyTiles)
                     heavy = __any_sync(0xffffffffu, ex2(fmaf(mt, c_u, -mc)) > kHeavyShare * (l * alpha));
@@ -621,7 +621,6 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         const float p0 = ex2(x01.x), p1 = ex2(x01.y), p2 = ex2(x23.x), p3 = ex2(x23.y);
                         lf[i & 3] = add2(lf[i & 3], add2(make_float2(p0, p1), make_float2(p2, p3)));
                         pw[i] = pack_e4m3x4(p0, p1, p2, p3);
-                        lq[i & 3] = add_e4m3x4(lq[i & 3], pw[i]);
                     }
                     uint32_t h0[16], h1[16];
 #pragma unroll
@@ -652,17 +651,18 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 const float2 lf01 = add2(lf[0], lf[1]), lf23 = add2(lf[2], lf[3]);
                 const float2 lfs = add2(lf01, lf23);
-                if constexpr (FP8 || kInlineSum) {
+                if constexpr (kInlineSum) {
                     lr = lr * alpha + ((lq[0] + lq[1]) + (lq[2] + lq[3]));
                 } else if constexpr (kHeavyTiles) {
-                    // d = 128: O is divided by lr, which must be the sum of the bf16 P the
-                    // MMA sees wherever few keys carry a row (a 2^-9 mismatch on a top
-                    // weight shows in O), while over many comparable keys the fp32 sum's
+                    // d = 128 (bf16 or E4M3 P): O is divided by lr, which must be the sum of
+                    // the rounded P the MMA sees wherever few keys carry a row (a mismatch
+                    // of the rounding step on a top weight shows in O: 2^-9 for bf16, 2^-4
+                    // for E4M3), while over many comparable keys the fp32 sum's
                     // rounding differences average out.  So the exact rounded sum is
                     // taken only in "heavy" tiles, where for some row of the warp the
                     // tile's largest P exceeds kHeavyShare of the row's running sum
                     // (always the unit's first tile): P is read back from tensor memory
-                    // and summed with mixed-precision adds.  Any key whose final weight
+                    // and summed exactly (mixed-precision adds; E4M3 decoded through f16).  Any key whose final weight
                     // exceeds kHeavyShare lies in a heavy tile.  Light tiles add their fp32
                     // sum.  (d = 64 gets the rounded sum from the MMA, column 64 of O; the
                     // key-split forward, whose variants run out of registers with this
@@ -670,13 +670,21 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     float add = lfs.x + lfs.y;
                     if (heavy) {
                         tmem_wait_st();
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
+                        if constexpr (FP8) {  // 32 columns of four E4M3 each
                             uint32_t r[32];
-                            tmem_ld32(tS + h * 32, r);
+                            tmem_ld32(tS, r);
                             tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) lq[i & 3] = add_bf16x2(lq[i & 3], r[i]);
+                            for (int i = 0; i < 32; ++i) lq[i & 3] = add_e4m3x4(lq[i & 3], r[i]);
+                        } else {  // 64 columns of two bf16 each
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                uint32_t r[32];
+                                tmem_ld32(tS + h * 32, r);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) lq[i & 3] = add_bf16x2(lq[i & 3], r[i]);
+                            }
                         }
                         add = (lq[0] + lq[1]) + (lq[2] + lq[3]);
                     }

@@ -3,11 +3,19 @@
 Inputs are the seeded bf16 workloads encoded per (b, h) with power-of-two
 scales (exact dequantisation), so the oracle runs on exactly the values the
 kernel multiplies.  The only approximation left is P rounded to E4M3 (3-bit
-mantissa, relative half-step 2^-4) for the P V product; a CPU simulation of
-that rounding on these workloads gives max |dO| up to 0.06 and mean |dO| up
-to 0.004, hence (with about a factor of two):
-    max |dO| <= 0.12,  mean |dO| <= 1e-2,  max |dLSE| <= 1e-3.
+mantissa, relative half-step 2^-4) for the P V product.  A CPU model of that
+rounding (tests/fp8_tolerance_sim.py, which follows the kernel's stale
+reference max and reproduces its errors to four digits) gives max |dO| up to
+0.078 and mean |dO| up to 0.004 on the cases below, hence (with about a
+factor of two):
+    max |dO| <= 0.12,  mean |dO| <= 1e-2,  max |dLSE| <= 1e-3,
+except on the 16x16x1000 large-logit cases checked on every row, where the
+model gives max |dO| 0.123 and 0.129 (rows carried by two keys whose E4M3
+weights both round): max |dO| <= 0.26 there.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -17,6 +25,7 @@ from exact_attention_32_gb300 import WORKLOADS, fa_get_device_status, forward_fp
 from exact_attention_32_gb300.workloads import quantize_e4m3, sample_rows
 
 MAX_O, MEAN_O, MAX_LSE = 0.12, 1e-2, 1e-3
+MAX_O_LARGE_LOGIT_ROWS = 0.26
 
 
 def test_quantization_is_exact_in_bf16():
@@ -37,10 +46,16 @@ def run(q, k, v, scale, causal):
     return o.double().cpu().numpy(), lse.double().cpu().numpy(), (qd, kd, vd)
 
 
-def check(o, lse, o_ref, lse_ref):
+def check(o, lse, o_ref, lse_ref, max_o=MAX_O):
     assert np.isfinite(o).all() and np.isfinite(lse).all()
     e, le = np.abs(o - o_ref), np.abs(lse - lse_ref)
-    assert e.max() <= MAX_O and e.mean() <= MEAN_O and le.max() <= MAX_LSE, (e.max(), e.mean(), le.max())
+    log = os.environ.get("FA_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"test": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0],
+                                "max_dO": float(e.max()), "mean_dO": float(e.mean()),
+                                "max_dLSE": float(le.max())}) + "\n")
+    assert e.max() <= max_o and e.mean() <= MEAN_O and le.max() <= MAX_LSE, (e.max(), e.mean(), le.max())
 
 
 @pytest.mark.gpu
@@ -71,6 +86,18 @@ def test_large_logits():
     o, lse, (qd, kd, vd) = run(q, k, v, 0.0883883461356163, True)
     o_ref, lse_ref = oracle.attention(qd, kd, vd, 0.0883883461356163, True)
     check(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True])
+def test_large_logits_every_row(causal):
+    # many rows carried by one or two keys, where the E4M3 rounding of P and the
+    # divisor of O matter most
+    q, k, v = make_inputs(16, 16, 1000, 128, seed=4200 + causal, q_gain=8.0)
+    scale = float(np.float32(1 / np.sqrt(128)))
+    o, lse, (qd, kd, vd) = run(q, k, v, scale, causal)
+    o_ref, lse_ref = oracle.attention(qd, kd, vd, scale, causal)
+    check(o, lse, o_ref, lse_ref, max_o=MAX_O_LARGE_LOGIT_ROWS)
 
 
 @pytest.mark.gpu
