@@ -598,7 +598,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     m_ref = m_new;
                 }
                 // P = exp2(s * scale * log2 e - m_ref * scale * log2 e), bf16, over the first 64 columns
-                // of S_t; fp32 and bf16-rounded row sums in independent partial accumulators
+                // of S_t; the fp32 row sum in partial accumulators (the divisor of O: see below)
                 const float mc = (m_ref == -INFINITY ? 0.f : m_ref) * c_u;
                 // how the divisor of O is summed at d = 128 (see the row sums below): every
                 // term inline in the key-split forward, else per tile as needed
@@ -725,13 +725,14 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             if (!ok || !(ok = mbar_wait_warp(bars.o_full(t), uc & 1, kWaitLimitNs))) break;
             tc_fence_after();
-            // epilogue: O = u / l in bf16 straight from registers to global memory.
-            // u was accumulated from bf16-rounded P, so it is divided by the sum of
-            // those same rounded terms: the weights then sum to one exactly and a
-            // row dominated by one key returns that key's value without a P-rounding
-            // error.  The next unit's first P V (which overwrites O_t) is issued
-            // only after this warpgroup's next p_full arrive, so the reads here are safe.
-            // a row with no admitted key in this split has l = 0: O = 0, LSE = -inf
+            // epilogue: O = u / lr in bf16 (fp32 for the key-split forward) straight
+            // from registers to global memory, LSE from the fp32 sum l.  u was built
+            // from the rounded P; lr sums those same rounded terms wherever one key
+            // can carry the row (see the row sums above; d = 64: column 64 of O), so
+            // such a row returns its key's value without a P-rounding error.  The next
+            // unit's first P V (which overwrites O_t) is issued only after this
+            // warpgroup's next p_full arrive, so the reads here are safe.  A row with
+            // no admitted key in this split has l = 0: O = 0, LSE = -inf.
             if constexpr (C::kOnesCol) {
                 lr = __uint_as_float(tmem_ld1(tO + 64));
                 tmem_wait_ld();
