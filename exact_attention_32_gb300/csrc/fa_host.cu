@@ -35,18 +35,37 @@ struct HostPipe {
 };
 HostPipe g_pipes[kMaxDevices];
 
+// Destroys whatever a failed create() made, so that a later call starts clean.
+void destroy(HostPipe &hp)
+{
+    for (int g = 0; g < kMaxGroups; ++g) {
+        if (hp.in[g]) cudaEventDestroy(hp.in[g]);
+        if (hp.comp[g]) cudaEventDestroy(hp.comp[g]);
+        hp.in[g] = hp.comp[g] = nullptr;
+    }
+    if (hp.start) cudaEventDestroy(hp.start);
+    if (hp.done) cudaEventDestroy(hp.done);
+    if (hp.s_in) cudaStreamDestroy(hp.s_in);
+    if (hp.s_out) cudaStreamDestroy(hp.s_out);
+    hp.start = hp.done = nullptr;
+    hp.s_in = hp.s_out = nullptr;
+}
+
 bool create(HostPipe &hp)
 {
     if (hp.ready) return true;
     const unsigned ef = cudaEventDisableTiming;
-    if (cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaStreamCreateWithFlags(&hp.s_out, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&hp.start, ef) != cudaSuccess || cudaEventCreateWithFlags(&hp.done, ef) != cudaSuccess)
+    bool ok = cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&hp.s_out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.start, ef) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.done, ef) == cudaSuccess;
+    for (int g = 0; g < kMaxGroups && ok; ++g)
+        ok = cudaEventCreateWithFlags(&hp.in[g], ef) == cudaSuccess &&
+             cudaEventCreateWithFlags(&hp.comp[g], ef) == cudaSuccess;
+    if (!ok) {
+        destroy(hp);
         return false;
-    for (int g = 0; g < kMaxGroups; ++g)
-        if (cudaEventCreateWithFlags(&hp.in[g], ef) != cudaSuccess ||
-            cudaEventCreateWithFlags(&hp.comp[g], ef) != cudaSuccess)
-            return false;
+    }
     hp.ready = true;
     return true;
 }
