@@ -117,7 +117,10 @@ __device__ __forceinline__ void report_timeout() { atomicExch(&g_tc_status, FA_E
 // Work item u: 256 consecutive query rows of one (b, h) slice against one key
 // split (keys [split * kv_chunk, (split + 1) * kv_chunk), a multiple of 128;
 // a single split covers all keys).  Items are ordered by row block, heaviest
-// causal block first, then by split.  CTA c of a persistent grid of G CTAs
+// causal block first, then by split.  Without key splits (and without a block
+// mask) the (b, h) slices go in groups of `hg` (all of one group's items before
+// the next group's), sized so that a group's K and V stay in L2 while its items
+// run.  CTA c of a persistent grid of G CTAs
 // takes, in round r, item r*G + c when r is even and r*G + (G-1-c) when r is
 // odd: the zigzag pairs heavy items with light ones, so every CTA ends up with
 // about the same number of K/V tiles without a shared counter.
@@ -192,13 +195,22 @@ __device__ __forceinline__ int unit_index(int r)
 // SPLIT: the launch covers key splits (the split-KV partials); otherwise every
 // item spans all N keys, and the split fields are compile-time constants, so
 // the single-split variants carry none of the key-range arithmetic.
-template <bool CAUSAL, bool SPLIT>
-__device__ __forceinline__ Unit unit_of(int u, int N, int BH, int n_mblocks, int n_splits, int kv_chunk)
+template <bool CAUSAL, bool SPLIT, bool GROUPED>
+__device__ __forceinline__ Unit unit_of(int u, int N, int BH, int n_mblocks, int n_splits, int kv_chunk, int hg)
 {
     Unit w;
     if constexpr (!SPLIT) {
-        const int mb = CAUSAL ? (n_mblocks - 1 - u / BH) : (u / BH);
-        w.bh = u % BH;
+        int mb;
+        if constexpr (GROUPED) {
+            // group g holds slices [g hg, min(BH, (g + 1) hg)); every group before it is full
+            const int g = u / (hg * n_mblocks), r = u - g * hg * n_mblocks;
+            const int nh = min(hg, BH - g * hg);
+            mb = CAUSAL ? (n_mblocks - 1 - r / nh) : (r / nh);
+            w.bh = g * hg + r % nh;
+        } else {
+            mb = CAUSAL ? (n_mblocks - 1 - u / BH) : (u / BH);
+            w.bh = u % BH;
+        }
         w.q_row0 = mb * (kQTiles * kBlockM);
         w.split = 0;
         w.kv_begin = 0;
@@ -235,7 +247,7 @@ template <int D, bool CAUSAL, bool OUT_F32, bool FP8, bool SPARSE>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, void *__restrict__ o, float *__restrict__ lse, int N,
-                 int BH, int n_mblocks, int n_units, int n_splits, int kv_chunk, float scale, float scale_log2,
+                 int BH, int n_mblocks, int n_units, int n_splits, int kv_chunk, int hg, float scale, float scale_log2,
                  const float *__restrict__ qs, const float *__restrict__ ks, const float *__restrict__ vs,
                  const uint8_t *__restrict__ bm, int nb)
 {
@@ -320,7 +332,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             bool ok = true;
             int it = 0, uc = 0;
             for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
-                const Unit w = unit_of<CAUSAL, OUT_F32>(u, N, BH, n_mblocks, n_splits, kv_chunk);
+                const Unit w = unit_of<CAUSAL, OUT_F32, !SPARSE>(u, N, BH, n_mblocks, n_splits, kv_chunk, hg);
                 if (!any_live(w)) continue;  // no admitted key: nothing to load
                 // the Q buffers are free once the previous unit's last S MMAs have completed
                 if (!mbar_wait(bars.q_empty(), (uc & 1) ^ 1, kWaitLimitNs)) {
@@ -405,7 +417,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             bool ok = true;
             int it = 0, uc = 0, jg = 0;  // ring position, units done, K/V tiles done (all units)
             for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
-                const Unit w = unit_of<CAUSAL, OUT_F32>(u, N, BH, n_mblocks, n_splits, kv_chunk);
+                const Unit w = unit_of<CAUSAL, OUT_F32, !SPARSE>(u, N, BH, n_mblocks, n_splits, kv_chunk, hg);
                 if (!any_live(w)) continue;
                 if (!(ok = mbar_wait(bars.q_full(), uc & 1, kWaitLimitNs))) break;
                 tc_fence_after();
@@ -501,7 +513,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         bool ok = true;
         int jg = 0, uc = 0;
         for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
-            const Unit w = unit_of<CAUSAL, OUT_F32>(u, N, BH, n_mblocks, n_splits, kv_chunk);
+            const Unit w = unit_of<CAUSAL, OUT_F32, !SPARSE>(u, N, BH, n_mblocks, n_splits, kv_chunk, hg);
             const int row_g = w.q_row0 + t * kBlockM + row;
             auto out_row_of = [&]() { return (static_cast<int64_t>(w.split) * BH + w.bh) * N + row_g; };
             const bool qb_ok = !SPARSE || (w.q_row0 / kBlockM + t < nb);
@@ -836,10 +848,20 @@ cudaError_t launch(const FaProblem &p, void *o, float *lse, int n_splits, int kv
     const int64_t n_units = n_mblocks * BH * n_splits;
     if (n_units > 0x7fffffffLL || BH > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int64_t grid = n_units < p.sm_count ? n_units : p.sm_count;  // persistent: one CTA per SM
+    // slices per group: when the K and V of all slices exceed 160 MB (L2: 129 MB),
+    // groups whose K and V take about 64 MB; else one group (grouping a working
+    // set that L2 already holds, or the few tiles a block-sparse unit reads, only
+    // costs balance)
+    const int64_t kv_bytes = 2 * p.N * p.d * C::kElem;
+    int64_t hg = BH;
+    if (!SPARSE && BH * kv_bytes > (int64_t(160) << 20)) {
+        hg = (int64_t(64) << 20) / kv_bytes;
+        hg = hg < 1 ? 1 : (hg > BH ? BH : hg);
+    }
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
     kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
         mq, mk, mv, o, lse, static_cast<int>(p.N), static_cast<int>(BH), static_cast<int>(n_mblocks),
-        static_cast<int>(n_units), n_splits, kv_chunk, p.scale, scale_log2, qs, ks, vs, bm,
+        static_cast<int>(n_units), n_splits, kv_chunk, static_cast<int>(hg), p.scale, scale_log2, qs, ks, vs, bm,
         static_cast<int>((p.N + kBlockN - 1) / kBlockN));
     return cudaGetLastError();
 }
