@@ -234,6 +234,16 @@ __device__ __forceinline__ Unit unit_of(int u, int N, int BH, int n_mblocks, int
     return w;
 }
 
+// Causal, all keys in one launch: a unit's last K/V tile starts at or past row
+// q_row0 + 128 whenever query tile 1 has rows (q_row0 + 128 < N), so it is
+// fully masked for query tile 0, which then skips it (its S, P and P V).  (The
+// E4M3 softmax keeps the plain loop: its registers are at the limit.)
+template <bool CAUSAL, bool SPLIT, bool SPARSE, bool FP8>
+__device__ __forceinline__ bool tile0_skips_last(const Unit &w, int N)
+{
+    return CAUSAL && !SPLIT && !SPARSE && !FP8 && w.q_row0 + kBlockM < N;
+}
+
 // OUT_F32: O is written as fp32 (the partial results of a key split) instead
 // of bf16; split s writes its rows at o + s * B*H*N*d and lse + s * B*H*N.
 // FP8: Q, K, V are E4M3 with one fp32 scale per (b, h) each (qs, ks, vs): the
@@ -415,7 +425,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const uint32_t dk_hi = static_cast<uint32_t>(dk0 >> 32), dv_hi = static_cast<uint32_t>(dv0 >> 32);
             constexpr uint32_t kTile16 = C::kTileBytes >> 4;
             bool ok = true;
-            int it = 0, uc = 0, jg = 0;  // ring position, units done, K/V tiles done (all units)
+            int it = 0, uc = 0;     // ring position, units done
+            int jg0 = 0, jg1 = 0;   // S tiles issued for query tile 0 / 1 (all units)
             for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
                 const Unit w = unit_of<CAUSAL, OUT_F32, !SPARSE>(u, N, BH, n_mblocks, n_splits, kv_chunk, hg);
                 if (!any_live(w)) continue;
@@ -424,6 +435,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 uint32_t prev_v_lo = 0;
                 int prev_v = -1;
                 int jj = 0;  // K/V tiles of this unit processed so far
+                const bool skip0 = tile0_skips_last<CAUSAL, OUT_F32, SPARSE, FP8>(w, N);
                 // (block-sparse: the producer's records give the live tiles; j only counts)
                 for (int j = 0; j < w.n_kv && ok; ++j) {
                     const int kslot = it % C::kStages, kuse = it / C::kStages;
@@ -435,8 +447,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     const uint32_t meta = SPARSE ? kv_meta[kslot] : 0u;
                     const uint32_t dk_lo = static_cast<uint32_t>(dk0) + kslot * kTile16;
                     for (int t = 0; t < kQTiles && ok; ++t) {
-                        if (jj > 0) {
-                            if (!(ok = mbar_wait(bars.p_full(t), (jg - 1) & 1, kWaitLimitNs))) break;
+                        if (jj > 0) {  // query tile t ran every tile before this one
+                            if (!(ok = mbar_wait(bars.p_full(t), ((t == 0 ? jg0 : jg1) - 1) & 1, kWaitLimitNs))) break;
                             tc_fence_after();
 #pragma unroll
                             for (int kk = 0; kk < C::kPVSteps; ++kk) {
@@ -449,6 +461,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                                 dv_hi, idO, (jj > 1 || kk > 0) ? 1u : 0u);
                             }
                         }
+                        if (t == 0 && skip0 && j == w.n_kv - 1) continue;  // fully masked for query tile 0
                         if constexpr (SPARSE)  // this S tile's record, for the softmax (published by the arrive below)
                             s_meta[t] = (meta & (kMetaTile | kMetaLast)) | (((meta >> (30 - t)) & 1u) << 30);
                         const uint32_t aq_lo = dq_lo + t * kTile16;
@@ -464,6 +477,10 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         }
                         mma_commit(bars.s_full(t));
                         if constexpr (SPARSE) mbar_arrive(bars.s_full(t));
+                        if (t == 0)
+                            ++jg0;
+                        else
+                            ++jg1;
                     }
                     if (!ok) break;
                     mma_commit(bars.empty(kslot));
@@ -474,14 +491,17 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     // d = 64: the block "after" V's 64 columns is the ones block, so the leading
                     // byte offset (bits 16..29) falls by what the start address (bits 0..13) gains
                     prev_v_lo = static_cast<uint32_t>(dv0) + vslot * (C::kOnesCol ? kTile16 - (kTile16 << 16) : kTile16);
-                    ++jg;
                     ++jj;
                     if (SPARSE && (meta & kMetaLast) != 0u) break;
                 }
                 if (!ok) break;
                 mma_commit(bars.q_empty());  // the last reads of this unit's Q are issued
                 for (int t = 0; t < kQTiles && ok; ++t) {
-                    if (!(ok = mbar_wait(bars.p_full(t), (jg - 1) & 1, kWaitLimitNs))) break;
+                    if (t == 0 && skip0) {  // its last P V went out with the unit's last tile
+                        mma_commit(bars.o_full(t));
+                        continue;
+                    }
+                    if (!(ok = mbar_wait(bars.p_full(t), ((t == 0 ? jg0 : jg1) - 1) & 1, kWaitLimitNs))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < C::kPVSteps; ++kk) {
@@ -557,7 +577,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             int jj = 0;  // K/V tiles of this unit processed so far
             // block-sparse: the loop counts the unit's live tiles; each one's index and
             // admission bit come with its S tile (the MMA thread's record)
-            for (int jc = 0; jc < w.n_kv; ++jc) {
+            const int n_mine = w.n_kv - (t == 0 && tile0_skips_last<CAUSAL, OUT_F32, SPARSE, FP8>(w, N) ? 1 : 0);
+            for (int jc = 0; jc < n_mine; ++jc) {
                 if (!mbar_wait_warp(bars.s_full(t), jg & 1, kWaitLimitNs)) {
                     ok = false;
                     break;
