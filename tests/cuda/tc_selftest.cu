@@ -62,8 +62,10 @@ tc_selftest_kernel(const uint16_t *q, const uint16_t *k, const uint16_t *v, floa
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t koff = (kk / 4) * (128 * 128) + (kk % 4) * 32;
-            mma_ss(tS, smem_desc_sw128(smem_u32(sQ) + koff, 16, 1024),
-                   smem_desc_sw128(smem_u32(sK) + koff, 16, 1024), idS, kk > 0);
+            const uint64_t da = smem_desc_sw128(smem_u32(sQ) + koff, 16, 1024);
+            const uint64_t db = smem_desc_sw128(smem_u32(sK) + koff, 16, 1024);
+            mma_ss_lohi(tS, static_cast<uint32_t>(da), static_cast<uint32_t>(da >> 32), static_cast<uint32_t>(db),
+                        static_cast<uint32_t>(db >> 32), idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(smem_u32(bar));
     }
@@ -98,8 +100,11 @@ tc_selftest_kernel(const uint16_t *q, const uint16_t *k, const uint16_t *v, floa
     if (tid == 0) {
         constexpr uint32_t idO = idesc_bf16_f32(128, D, true);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tO, tS + kk * 8, smem_desc_sw128(smem_u32(sV) + kk * 16 * 128, 128 * 128, 1024), idO, kk > 0);
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t dv = smem_desc_sw128(smem_u32(sV) + kk * 16 * 128, 128 * 128, 1024);
+            mma_ts_lohi(tO, tS + kk * 8, static_cast<uint32_t>(dv), static_cast<uint32_t>(dv >> 32), idO,
+                        kk > 0 ? 1u : 0u);
+        }
         mma_commit(smem_u32(bar));
     }
     __syncwarp();
