@@ -229,8 +229,10 @@ int fa_fwd_blocksparse(const void *q, const void *k, const void *v, void *o, flo
  *   o         : bf16 out [B, H, N, d];  lse : fp32 out [B, H, N]
  *   d         : 128 only (else FA_ERR_UNSUPPORTED)
  * Other arguments and errors as fa_fwd.  Accuracy is set by E4M3's 3-bit
- * mantissa on P (O is divided by the sum of the rounded P, so the weights
- * still sum to one); LSE uses the unrounded sum.
+ * mantissa on P.  O is divided by the sum of the rounded P over every tile in
+ * which one key can carry a quarter of the row, so the weights of a row that
+ * few keys dominate still sum to one.  Elsewhere it is divided by the fp32
+ * sum, whose rounding differences average out.  LSE uses the unrounded sum.
  */
 int fa_fwd_fp8(const void *q, const void *k, const void *v, const float *q_scale,
                const float *k_scale, const float *v_scale, void *o, float *lse,
