@@ -8,9 +8,14 @@ inputs resident in device memory.  The default workload is the long causal
 run B=1, H=32, N=16384, d=128.  Q/K/V (402 MB) plus O (134 MB) exceed the
 129 MB L2, so consecutive steps do not run from a warm L2.
 
-Under torchrun (N > 1) every rank runs the same workload on its own GPU
-(independent replicas, weak scaling; no collective touches the data; a barrier
-and a max-reduce of the timings only).
+Under torchrun (N > 1) the job is sharded over the ranks by (b, h) slices:
+rank r takes the contiguous slab fa_bh_partition(B*H, N, r) and runs fa_fwd
+on it on its own GPU.  The slices are independent, so no collective touches
+the data (a barrier and a max-reduce of the timings only).  ``--scaling
+weak`` (default): the job is N draws of the workload (draw r from seed
+seed + r, draw 0 the workload itself), B*H*N slices in all, so every rank
+keeps the workload's size.  ``--scaling strong``: the job is the workload
+itself, its B*H slices split over the ranks.
 
 ``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample of
 rows of the same workload, and reports the same metric for it.
@@ -55,6 +60,9 @@ def parse_args():
                         "mma = fa_fwd_mma (the warp-level mma.sync kernel, kept as a baseline)")
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="target CPU time of the oracle baseline sample")
+    p.add_argument("--scaling", default="weak", choices=["weak", "strong"],
+                   help="under torchrun: weak = N draws of the workload, one slab of B*H slices per rank; "
+                        "strong = the workload's B*H slices split over the ranks")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-secondary", action="store_true",
@@ -93,6 +101,25 @@ def max_over_ranks(x: float, world: int) -> float:
     t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def slab_inputs(w, world: int, rank: int, scaling: str):
+    """This rank's part of the job: (local shape (B, H, N, d), CPU inputs
+    (q, k, v) of that shape, FLOPs of the whole job, slab (begin, count) in
+    the job's (b, h) slices).  The slab comes from the library's
+    fa_bh_partition."""
+    import exact_attention_32_gb300 as fa
+    BH = w.B * w.H
+    if scaling == "weak":
+        # the job: `world` draws of the workload stacked along the batch (draw r
+        # from seed + r); rank r's slab is exactly draw r
+        begin, count = fa.fa_bh_partition(world * BH, world, rank)
+        assert begin == rank * BH and count == BH
+        inputs = workload_inputs(w, seed=w.seed + rank)
+        return (w.B, w.H, w.N, w.d), inputs, w.flops * world, (begin, count)
+    begin, count = fa.fa_bh_partition(BH, world, rank)
+    q, k, v = (t.reshape(1, BH, w.N, w.d)[:, begin:begin + count].contiguous() for t in workload_inputs(w))
+    return (1, count, w.N, w.d), (q, k, v), w.flops, (begin, count)
 
 
 # ---------------------------------------------------------------------- peaks
@@ -400,19 +427,23 @@ def run_ours(args, rank, world, local):
     w = WORKLOADS[args.workload]
     dev = torch.device("cuda", local if world > 1 else 0)
     fa.lib()
-    q_h, k_h, v_h = workload_inputs(w)
+    (Bl, Hl, N, d), (q_h, k_h, v_h), job_flops, slab = slab_inputs(w, world, rank, args.scaling)
+    local_flops = w.flops / (w.B * w.H) * Bl * Hl  # this rank's share
     q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
     o = torch.empty_like(q)
-    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+    lse = torch.empty(Bl, Hl, N, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr())
+    busy = Bl * Hl > 0  # a strong-scaling rank past the last slice has nothing to run
 
     fwd = fa.fa_fwd if args.kernel == "tc" else fa.fa_fwd_mma
     kernel_name = "fa_fwd_tc_kernel" if args.kernel == "tc" else "fa_fwd_mma_kernel"
 
     def step():
-        st = fwd(*ptrs, w.B, w.H, w.N, w.d, w.scale, w.causal, sp)
+        if not busy:
+            return
+        st = fwd(*ptrs, Bl, Hl, N, d, w.scale, w.causal, sp)
         if st != 0:
             raise fa.FAError(st, "fa_fwd" if args.kernel == "tc" else "fa_fwd_mma")
 
@@ -435,8 +466,8 @@ def run_ours(args, rank, world, local):
         time.sleep(0.3)
     # inputs smaller than L2 are evicted between steps by writing a 256 MB
     # buffer (outside the per-launch events; `value` then comes from those)
-    io_bytes = 4 * w.B * w.H * w.N * w.d * 2
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if io_bytes < 2 * L2_BYTES else None
+    io_bytes = 4 * Bl * Hl * N * d * 2
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if busy and io_bytes < 2 * L2_BYTES else None
     e0.record(stream)
     for i in range(K):
         if flush is not None:
@@ -460,14 +491,14 @@ def run_ours(args, rank, world, local):
 
     if flush is not None:  # the timed region also holds the flushes: count the launches only
         total_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)), world)
-    value = w.flops * K * world / (total_ms / 1e3) / 1e12
+    value = job_flops * K / (total_ms / 1e3) / 1e12
 
     # end to end through the C ABI with host buffers (fa_fwd_host): pinned host
     # Q, K, V in, O and LSE out, every copy inside the timed region; the
     # library overlaps the copies of one group of (b, h) slices with the
     # forward of another
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and busy:
         qp, kp, vp_ = (t.pin_memory() for t in (q_h, k_h, v_h))
         op = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
         lp = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
@@ -491,7 +522,7 @@ def run_ours(args, rank, world, local):
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
         in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
         out_bytes = o.numel() * o.element_size() + lse.numel() * lse.element_size()
-        e2e = {"value": w.flops * Ke * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_flops * Ke / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
                "steps": Ke, "ms_per_step": e2e_ms / Ke,
                "api": "fa_fwd_host (pinned host buffers, copies overlapped over 4 groups of (b, h) slices)"}
@@ -500,15 +531,17 @@ def run_ours(args, rank, world, local):
         return None
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
-    achieved = w.flops / (launch_ms / 1e3) / 1e12
+    achieved = local_flops / (launch_ms / 1e3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": args.scaling, "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: Q, K, V iid N(0,1) fp32 rounded to bf16, seeded",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-                   "causal": w.causal, "scale": w.scale, "global_batch": w.B * world,
-                   "seq_len": w.N, "parallelism": f"replicas{world}",
+                   "causal": w.causal, "scale": w.scale,
+                   "global_batch": w.B * world if args.scaling == "weak" else w.B,
+                   "seq_len": w.N, "parallelism": f"bh_slabs{world}",
+                   "slab_rank0": {"begin": slab[0], "count": slab[1]},
                    "l2": ("inputs larger than L2 (Q+K+V+O exceed 2 x 129 MB), no flush" if flush is None else
                           "L2 flushed between steps (256 MB write, outside the per-launch events); "
                           "value from the per-launch event times")},
@@ -516,9 +549,9 @@ def run_ours(args, rank, world, local):
         "roofline": {"bound": "tensor", "kernel": kernel_name, "achieved": achieved,
                      "peak": peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
                      "unit": "TFLOP/s", "frac": achieved / peak,
-                     "traffic": load_traffic(kernel_name, w.name),
-                     "algorithmic_flops_per_launch": w.flops,
-                     "algorithmic_bytes_per_launch": w.min_bytes,
+                     "traffic": load_traffic(kernel_name, w.name) if Bl * Hl == w.B * w.H else None,
+                     "algorithmic_flops_per_launch": local_flops,
+                     "algorithmic_bytes_per_launch": w.min_bytes // (w.B * w.H) * Bl * Hl,
                      "launch_ms": launch_ms},
         "gpu_launches": K,
         "launch_ms_percentiles": pct,

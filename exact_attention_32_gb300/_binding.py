@@ -23,7 +23,7 @@ _lock = threading.Lock()
 FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_NO_DEVICE",
                 4: "FA_ERR_ARCH", 5: "FA_ERR_LAUNCH", 6: "FA_ERR_TIMEOUT", 7: "FA_ERR_WORKSPACE_LIMIT"}
-EXPORTED = ("fa_fwd", "fa_fwd_host", "fa_fwd_mma", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_combine",
+EXPORTED = ("fa_fwd", "fa_bh_partition", "fa_fwd_slab", "fa_fwd_host", "fa_fwd_mma", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_combine",
             "fa_fwd_splitkv_noalloc", "fa_fwd_fp8", "fa_fwd_blocksparse", "fa_bwd", "fa_bwd_workspace_bytes", "fa_get_device_status",
             "fa_status_string", "fa_version")
 
@@ -47,6 +47,11 @@ def lib():
             L.fa_fwd.restype = ctypes.c_int
             L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
                                  ctypes.c_int, vp]
+            L.fa_bh_partition.restype = ctypes.c_int
+            L.fa_bh_partition.argtypes = [i64, i64, i64, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+            L.fa_fwd_slab.restype = ctypes.c_int
+            L.fa_fwd_slab.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float, ctypes.c_int,
+                                      i64, i64, vp]
             L.fa_fwd_host.restype = ctypes.c_int
             L.fa_fwd_host.argtypes = [vp] * 10 + [i64, i64, i64, i64, ctypes.c_float, ctypes.c_int, i64, vp]
             L.fa_fwd_mma.restype = ctypes.c_int
@@ -83,6 +88,22 @@ def lib():
 def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
     """Raw call: pointers as ints, ``stream`` a cudaStream_t as int (0 = legacy default)."""
     return lib().fa_fwd(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), int(causal), stream)
+
+
+def fa_bh_partition(n_slices: int, world: int, rank: int):
+    """(begin, count): the contiguous slab of (b, h) slices rank ``rank`` of
+    ``world`` takes (pure host computation in the library).  Raises FAError
+    on invalid arguments."""
+    begin, count = ctypes.c_int64(0), ctypes.c_int64(0)
+    st = lib().fa_bh_partition(int(n_slices), int(world), int(rank), ctypes.byref(begin), ctypes.byref(count))
+    if st != FA_OK:
+        raise FAError(st, "fa_bh_partition")
+    return begin.value, count.value
+
+
+def fa_fwd_slab(q, k, v, o, lse, B, H, N, d, scale, causal, rank, world, stream) -> int:
+    """Raw call of the forward over one rank's slab of a [B, H, N, d] problem."""
+    return lib().fa_fwd_slab(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), int(causal), rank, world, stream)
 
 
 def fa_fwd_host(q, k, v, o, lse, q_dev, k_dev, v_dev, o_dev, lse_dev, B, H, N, d, scale, causal, n_groups,

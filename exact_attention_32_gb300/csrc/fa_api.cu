@@ -45,11 +45,12 @@ int current_device(int *dev, int *sm_count)
     return info.status;
 }
 
-// A pointer the kernels may dereference: 16-byte aligned device (or managed)
-// memory of the current device.
-int check_pointer(const void *p, int dev)
+// A pointer the kernels may dereference: device (or managed) memory of the
+// current device, aligned to `align` bytes (16 unless the kernels only make
+// scalar 4-byte accesses through it).
+int check_pointer(const void *p, int dev, uintptr_t align = 16)
 {
-    if (p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) != 0) return FA_ERR_INVALID_ARG;
+    if (p == nullptr || (reinterpret_cast<uintptr_t>(p) & (align - 1)) != 0) return FA_ERR_INVALID_ARG;
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
         cudaGetLastError();
@@ -80,8 +81,9 @@ bool overlaps(const void *a, uint64_t na, const void *b, uint64_t nb)
 
 typedef cudaError_t (*Launcher)(const FaProblem &, cudaStream_t);
 
-// Sizes of an attention problem; pure host logic, no CUDA call.
-int check_sizes(int64_t B, int64_t H, int64_t N, int64_t d)
+}  // namespace
+
+int fa_check_sizes(int64_t B, int64_t H, int64_t N, int64_t d)
 {
     if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
     if (N > (int64_t(1) << 31) - 256 || B > (int64_t(1) << 31) || H > (int64_t(1) << 31))
@@ -91,28 +93,27 @@ int check_sizes(int64_t B, int64_t H, int64_t N, int64_t d)
     return FA_OK;
 }
 
-constexpr int64_t kMaxSplits = 32;
-
-// Key-split geometry of fa_fwd_splitkv: chunks of a multiple of 128 keys, no empty chunk.
-void split_geometry(int64_t N, int64_t n_splits, int64_t *chunk, int64_t *parts)
+void fa_split_geometry(int64_t N, int64_t n_splits, int64_t *chunk, int64_t *parts)
 {
     const int64_t per = (N + n_splits - 1) / n_splits;
     *chunk = (per + 127) / 128 * 128;
     *parts = (N + *chunk - 1) / *chunk;
 }
 
-int64_t splitkv_bytes(int64_t B, int64_t H, int64_t N, int64_t d, int64_t n_splits)
+int64_t fa_splitkv_bytes(int64_t B, int64_t H, int64_t N, int64_t d, int64_t n_splits)
 {
     int64_t chunk, parts;
-    split_geometry(N, n_splits, &chunk, &parts);
+    fa_split_geometry(N, n_splits, &chunk, &parts);
     return parts * B * H * N * (d + 1) * 4;
 }
+
+namespace {
 
 int validate_and_launch(Launcher launch, const void *q, const void *k, const void *v, void *o, float *lse,
                         int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal, void *stream)
 {
     // sizes first: nothing is touched for an invalid problem
-    int st = check_sizes(B, H, N, d);
+    int st = fa_check_sizes(B, H, N, d);
     if (st != FA_OK) return st;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
@@ -120,9 +121,10 @@ int validate_and_launch(Launcher launch, const void *q, const void *k, const voi
     int dev = 0, sm_count = 0;
     st = current_device(&dev, &sm_count);
     if (st != FA_OK) return st;
-    const void *ptrs[5] = {q, k, v, o, lse};
+    const void *ptrs[4] = {q, k, v, o};
     for (const void *p : ptrs)
         if ((st = check_pointer(p, dev)) != FA_OK) return st;
+    if ((st = check_pointer(lse, dev, 4)) != FA_OK) return st;  // written by scalar stores only
 
     const uint64_t tbytes = static_cast<uint64_t>(B * H * N * d) * 2u;
     const uint64_t lbytes = static_cast<uint64_t>(B * H * N) * 4u;
@@ -156,11 +158,40 @@ extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, floa
     return validate_and_launch(fa_launch_tc, q, k, v, o, lse, B, H, N, d, scale, causal, stream);
 }
 
+extern "C" int fa_bh_partition(int64_t n_slices, int64_t world, int64_t rank, int64_t *begin, int64_t *count)
+{
+    if (n_slices < 0 || world < 1 || rank < 0 || rank >= world || begin == nullptr || count == nullptr)
+        return FA_ERR_INVALID_ARG;
+    // the first n_slices % world ranks take one slice more than the others
+    const int64_t base = n_slices / world, extra = n_slices % world;
+    *begin = rank * base + (rank < extra ? rank : extra);
+    *count = base + (rank < extra ? 1 : 0);
+    return FA_OK;
+}
+
+extern "C" int fa_fwd_slab(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                           int64_t H, int64_t N, int64_t d, float scale, int causal, int64_t rank, int64_t world,
+                           void *stream)
+{
+    int st = fa_check_sizes(B, H, N, d);
+    if (st != FA_OK) return st;
+    int64_t begin = 0, count = 0;
+    if ((st = fa_bh_partition(B * H, world, rank, &begin, &count)) != FA_OK) return st;
+    if ((causal != 0 && causal != 1) || !(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (count == 0) return FA_OK;  // more ranks than slices: nothing for this one
+    // the slab is itself a contiguous problem of `count` slices: B = 1, H = count
+    const int64_t t_off = begin * N * d * 2, l_off = begin * N;
+    auto at = [&](const void *p) { return static_cast<const void *>(static_cast<const char *>(p) + t_off); };
+    return validate_and_launch(fa_launch_tc, q ? at(q) : q, k ? at(k) : k, v ? at(v) : v,
+                               o ? const_cast<void *>(at(o)) : o, lse ? lse + l_off : lse, 1, count, N, d, scale,
+                               causal, stream);
+}
+
 extern "C" int fa_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse, void *q_dev,
                            void *k_dev, void *v_dev, void *o_dev, float *lse_dev, int64_t B, int64_t H, int64_t N,
                            int64_t d, float scale, int causal, int64_t n_groups, void *stream)
 {
-    int st = check_sizes(B, H, N, d);
+    int st = fa_check_sizes(B, H, N, d);
     if (st != FA_OK) return st;
     if ((causal != 0 && causal != 1) || !(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
     const int64_t BH = B * H;
@@ -218,19 +249,19 @@ extern "C" int fa_fwd_mma(const void *q, const void *k, const void *v, void *o, 
 
 extern "C" int64_t fa_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, int64_t n_splits)
 {
-    if (check_sizes(B, H, N, d) != FA_OK || n_splits < 1 || n_splits > kMaxSplits) return -1;
-    return splitkv_bytes(B, H, N, d, n_splits);
+    if (fa_check_sizes(B, H, N, d) != FA_OK || n_splits < 1 || n_splits > kFaMaxSplits) return -1;
+    return fa_splitkv_bytes(B, H, N, d, n_splits);
 }
 
 extern "C" int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
                               int64_t H, int64_t N, int64_t d, float scale, int causal, int64_t n_splits,
                               void *workspace, int64_t workspace_bytes, void *stream)
 {
-    int st = check_sizes(B, H, N, d);
+    int st = fa_check_sizes(B, H, N, d);
     if (st != FA_OK) return st;
     if ((causal != 0 && causal != 1) || !(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
-    if (n_splits < 1 || n_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
-    const int64_t need = splitkv_bytes(B, H, N, d, n_splits);
+    if (n_splits < 1 || n_splits > kFaMaxSplits) return FA_ERR_INVALID_ARG;
+    const int64_t need = fa_splitkv_bytes(B, H, N, d, n_splits);
     if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
 
     int dev = 0, sm_count = 0;
@@ -263,7 +294,7 @@ extern "C" int fa_fwd_splitkv(const void *q, const void *k, const void *v, void 
     p.causal = causal;
     p.sm_count = sm_count;
     int64_t chunk, parts;
-    split_geometry(N, n_splits, &chunk, &parts);
+    fa_split_geometry(N, n_splits, &chunk, &parts);
     const int64_t rows = B * H * N;
     float *o_parts = static_cast<float *>(workspace);
     float *lse_parts = o_parts + parts * rows * d;
@@ -278,9 +309,9 @@ extern "C" int fa_fwd_splitkv(const void *q, const void *k, const void *v, void 
 extern "C" int fa_combine(const float *o_parts, const float *lse_parts, int64_t n_parts, void *o, float *lse,
                           int64_t B, int64_t H, int64_t N, int64_t d, void *stream)
 {
-    int st = check_sizes(B, H, N, d);
+    int st = fa_check_sizes(B, H, N, d);
     if (st != FA_OK) return st;
-    if (n_parts < 1 || n_parts > kMaxSplits) return FA_ERR_INVALID_ARG;
+    if (n_parts < 1 || n_parts > kFaMaxSplits) return FA_ERR_INVALID_ARG;
     int dev = 0, sm_count = 0;
     if ((st = current_device(&dev, &sm_count)) != FA_OK) return st;
     const void *ptrs[4] = {o_parts, lse_parts, o, lse};
@@ -305,7 +336,7 @@ extern "C" int fa_fwd_blocksparse(const void *q, const void *k, const void *v, v
                                   int64_t H, int64_t N, int64_t d, float scale, int causal,
                                   const uint8_t *block_mask, void *stream)
 {
-    int st = check_sizes(B, H, N, d);
+    int st = fa_check_sizes(B, H, N, d);
     if (st != FA_OK) return st;
     if ((causal != 0 && causal != 1) || !(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
     int dev = 0, sm_count = 0;
@@ -342,7 +373,7 @@ extern "C" int fa_fwd_fp8(const void *q, const void *k, const void *v, const flo
                           const float *k_scale, const float *v_scale, void *o, float *lse, int64_t B, int64_t H,
                           int64_t N, int64_t d, float scale, int causal, void *stream)
 {
-    int st = check_sizes(B, H, N, d);
+    int st = fa_check_sizes(B, H, N, d);
     if (st != FA_OK) return st;
     if (d != 128) return FA_ERR_UNSUPPORTED;
     if ((causal != 0 && causal != 1) || !(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
@@ -379,7 +410,7 @@ extern "C" int fa_fwd_fp8(const void *q, const void *k, const void *v, const flo
 
 extern "C" int64_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d)
 {
-    if (check_sizes(B, H, N, d) != FA_OK) return -1;
+    if (fa_check_sizes(B, H, N, d) != FA_OK) return -1;
     return fa_bwd_workspace_size(B, H, N, d);
 }
 
@@ -387,7 +418,7 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
                       const void *dout, void *dq, void *dk, void *dv, int64_t B, int64_t H, int64_t N, int64_t d,
                       float scale, int causal, void *workspace, int64_t workspace_bytes, void *stream)
 {
-    int st = check_sizes(B, H, N, d);
+    int st = fa_check_sizes(B, H, N, d);
     if (st != FA_OK) return st;
     if ((causal != 0 && causal != 1) || !(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
     const int64_t need = fa_bwd_workspace_size(B, H, N, d);

@@ -21,6 +21,16 @@ cudaError_t set_max_dynamic_smem(int bytes)
     return e;
 }
 
+// Size rules shared by the entry points (pure host logic, no CUDA call):
+// FA_OK, FA_ERR_INVALID_ARG (sizes out of range) or FA_ERR_UNSUPPORTED (d).
+int fa_check_sizes(int64_t B, int64_t H, int64_t N, int64_t d);
+// Largest n_splits of fa_fwd_splitkv (and n_parts of fa_combine).
+constexpr int64_t kFaMaxSplits = 32;
+// Key-split geometry of fa_fwd_splitkv: chunks of a multiple of 128 keys, no empty chunk.
+void fa_split_geometry(int64_t N, int64_t n_splits, int64_t *chunk, int64_t *parts);
+// Workspace bytes of fa_fwd_splitkv for valid sizes and n_splits.
+int64_t fa_splitkv_bytes(int64_t B, int64_t H, int64_t N, int64_t d, int64_t n_splits);
+
 // One validated forward problem: contiguous [B, H, N, d] bf16 tensors.
 struct FaProblem {
     const void *q, *k, *v;

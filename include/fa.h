@@ -68,8 +68,10 @@ enum fa_status {
  *   causal  : 0 = every key admitted; 1 = key j admitted to query i iff j <= i.
  *   stream  : cudaStream_t to enqueue on.
  *
- * Every pointer must be 16-byte aligned and on the current device; o and lse
- * must not overlap q, k, v or each other.  Work is split into tiles of 128
+ * Every pointer must be on the current device; q, k, v and o 16-byte
+ * aligned, lse 4-byte aligned (it is written by scalar stores only, so the
+ * LSE of any run of whole rows can be addressed); o and lse must not overlap
+ * q, k, v or each other.  Work is split into tiles of 128
  * query rows; ragged N (not a multiple of the tile) is handled in the kernel.
  * Returns FA_OK or an fa_status code; an error found inside the kernel is
  * reported later by fa_get_device_status().
@@ -77,6 +79,41 @@ enum fa_status {
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
            void *stream);
+
+/*
+ * fa_bh_partition - the (b, h) slices one GPU of a sharded problem takes.
+ * The programs over (b, h) slices are independent and exchange nothing
+ * ("6.1 FlashAttention V1 in detail", section 8.2, the parallel partition),
+ * so a problem is spread over `world` GPUs by giving rank r a contiguous
+ * slab of slices [begin, begin + count): the first n_slices % world ranks take
+ * ceil(n_slices / world) slices, the others floor(n_slices / world).  Every
+ * slice belongs to exactly one rank; a rank past n_slices gets count = 0.
+ * Slices are numbered b * H + h, the order of the [B, H, N, d] layout, so a
+ * slab is one contiguous range of Q, K, V, O and LSE.
+ *
+ *   n_slices : B * H (>= 0)
+ *   world    : number of ranks (>= 1);  rank : 0 <= rank < world
+ *   begin, count : host outputs
+ * Pure host computation.  Returns FA_OK, or FA_ERR_INVALID_ARG (nothing
+ * written) for out-of-range arguments or a null output pointer.
+ */
+int fa_bh_partition(int64_t n_slices, int64_t world, int64_t rank, int64_t *begin,
+                    int64_t *count);
+
+/*
+ * fa_fwd_slab - fa_fwd over the slab of (b, h) slices that fa_bh_partition
+ * gives rank `rank` of `world`: q, k, v, o, lse are the whole problem's
+ * tensors, as for fa_fwd, and only the slab's rows of Q, K, V are read and
+ * only its rows of O and LSE written (the slab runs as a problem of B = 1,
+ * H = count).  Ranks on different GPUs that call it over the same problem
+ * (each with the tensors in its own memory) together compute all of it, with
+ * no communication.  A rank whose slab is empty launches nothing and returns
+ * FA_OK.  Errors as fa_fwd, plus FA_ERR_INVALID_ARG for a bad rank or world;
+ * pointers are checked at the slab's offset.
+ */
+int fa_fwd_slab(const void *q, const void *k, const void *v, void *o, float *lse,
+                int64_t B, int64_t H, int64_t N, int64_t d, float scale, int causal,
+                int64_t rank, int64_t world, void *stream);
 
 /*
  * fa_fwd_host - fa_fwd on HOST buffers: copies Q, K, V to the device, runs
@@ -169,15 +206,20 @@ int64_t fa_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t 
  * tensors, latency-critical loops that cannot afford a cudaMalloc).
  *
  * Arguments, result and errors are those of fa_fwd_splitkv without the
- * workspace: the parts go to a static device array of
- * FA_SPLITKV_NOALLOC_MAX_BYTES (32 MiB) that every GPU loading the library
- * holds until the process exits.  A problem whose
+ * workspace, checked in the same order: the parts go to a static device
+ * array of FA_SPLITKV_NOALLOC_MAX_BYTES (32 MiB) that every GPU loading the
+ * library holds until the process exits.  A valid problem whose
  * fa_fwd_splitkv_workspace_bytes(...) exceeds it is refused with
- * FA_ERR_WORKSPACE_LIMIT (nothing launched or written).  The first call on a
- * device looks up the array's device address (make it before any stream
- * capture).  No call allocates or frees device memory.  All calls share the
- * array: calls whose kernels can overlap on the GPU (unordered streams) race
- * and give undefined results.
+ * FA_ERR_WORKSPACE_LIMIT (nothing launched or written).  The array's device
+ * address belongs to the CUDA context current at the call: a call outside a
+ * stream capture looks it up in that context (and records it), a call on a
+ * stream being captured uses the address recorded for the current context.
+ * So make one call in each context (per device, and per context a host
+ * program creates itself) before any stream capture, and again after a
+ * cudaDeviceReset; a captured call with nothing recorded for its context
+ * returns FA_ERR_LAUNCH.  No call allocates or frees device memory.  All
+ * calls share the array: calls whose kernels can overlap on the GPU
+ * (unordered streams) race and give undefined results.
  */
 int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
                            int64_t B, int64_t H, int64_t N, int64_t d, float scale,

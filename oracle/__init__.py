@@ -34,6 +34,9 @@ Independent references, each in fp64 or better:
                        (query block, key block) pairs: keys of a masked block
                        take no part for the rows of that query block (numpy fp64,
                        dense per slice).
+``attention_probs``    the softmax weights P themselves (numpy fp64, plain
+                       definition, for selected rows): what the E4M3 forward's
+                       error bound is computed from.
 ``attention_decimal``  brute force in Python ``decimal`` at 50 digits, using
                        the softmax definition directly (exp(s_j) / sum exp(s_k),
                        no max shift) - an independent formulation for tiny
@@ -323,6 +326,27 @@ def attention_blocksparse(q, k, v, scale: float, causal: bool, block_mask, block
             o[b, h, live] = (E / l) @ vd[b, h]       # pass 3
             lse[b, h, live] = (m + np.log(l))[:, 0]
     return o, lse
+
+
+def attention_probs(q, k, scale: float, causal: bool, rows):
+    """The softmax weights P of the plain definition ("6.1 FlashAttention V1 in
+    detail", section 1.1: S = scale * Q K^T, P = softmax(S) row-wise), fp64,
+    for the flat row ids ``rows`` ((b*H + h)*N + i).  Masked keys (j > i when
+    causal) get weight 0.  Returns float64 numpy [len(rows), N]."""
+    qd, kd = _as_f64(q), _as_f64(k)
+    B, H, N, d = qd.shape
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.zeros((rows.size, N))
+    bh_of, i_of = np.divmod(rows, N)
+    for bh in np.unique(bh_of):
+        sel = np.nonzero(bh_of == bh)[0]
+        b, h = divmod(int(bh), H)
+        s = scale * (qd[b, h, i_of[sel]] @ kd[b, h].T)      # scores of these rows
+        if causal:
+            s[np.arange(N)[None, :] > i_of[sel][:, None]] = -np.inf
+        e = np.exp(s - s.max(axis=1, keepdims=True))
+        out[sel] = e / e.sum(axis=1, keepdims=True)
+    return out
 
 
 def attention_decimal(q, k, v, scale, causal: bool, digits: int = 50):

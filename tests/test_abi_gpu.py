@@ -44,6 +44,16 @@ def test_misaligned_pointer(bufs):
     assert untouched(o, lse)
 
 
+def test_lse_needs_only_four_byte_alignment(bufs):
+    q, o, lse, (B, H, N, d) = bufs
+    big = torch.full((B * H * N + 4,), 7.0, device="cuda")
+    assert raw(q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(), big.data_ptr() + 2, B, H, N, d) == 1
+    assert untouched(o, lse)
+    assert raw(q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(), big.data_ptr() + 4, B, H, N, d) == 0
+    torch.cuda.synchronize()
+    assert bool((big[0] == 7.0)) and bool(torch.isfinite(big[1:1 + B * H * N]).all()) and bool((big[-3:] == 7.0).all())
+
+
 def test_null_pointer(bufs):
     q, o, lse, (B, H, N, d) = bufs
     assert raw(0, q.data_ptr(), q.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d) == 1

@@ -451,3 +451,40 @@ def test_dense_matches_library_softmax_at_workload_size(name, head):
     lse_lib = logsumexp(s, axis=1)
     assert np.allclose(o[0, 0], o_lib, rtol=1e-12, atol=1e-12)
     assert np.allclose(lse[0, 0], lse_lib, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- probabilities
+
+def test_probs_worked_example():
+    # scores [2, 1, 0] (q = 1, scale 1): P = e^s / sum e^s, and P . values is
+    # the printed output
+    g, q, k, v = worked_example_inputs()
+    P = oracle.attention_probs(q, k, 1.0, False, rows=[0])[0]
+    e = np.exp(np.asarray(g["scores"]))
+    assert np.allclose(P, e / e.sum(), rtol=0, atol=1e-15)
+    assert abs(P @ np.asarray(g["values"]) - g["output"][0]) <= 0.5 * 10 ** -int(g["digits"][0])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_probs_times_v_is_the_dense_output(causal):
+    q, k, v = make_inputs(2, 3, 77, 64, seed=61, q_gain=3.0)
+    rows = np.arange(2 * 3 * 77)
+    P = oracle.attention_probs(q, k, 0.125, causal, rows)
+    assert np.allclose(P.sum(axis=1), 1.0, rtol=0, atol=1e-13)
+    if causal:
+        i = rows % 77
+        assert all((P[n, i[n] + 1:] == 0).all() for n in range(rows.size))
+    o_ref, _ = oracle.attention(q, k, v, 0.125, causal)
+    vd = v.double().numpy().reshape(6, 77, 64)
+    o = np.stack([P[n] @ vd[n // 77] for n in range(rows.size)])
+    assert np.abs(o - o_ref.reshape(-1, 64)).max() < 1e-12
+
+
+def test_probs_match_library_softmax():
+    from scipy.special import softmax
+    q, k, _ = make_inputs(1, 2, 50, 128, seed=62)
+    P = oracle.attention_probs(q, k, 0.0883883461356163, False, rows=[0, 49, 50, 99])
+    qd, kd = q.double().numpy(), k.double().numpy()
+    for n, (h, i) in enumerate([(0, 0), (0, 49), (1, 0), (1, 49)]):
+        ref = softmax(0.0883883461356163 * (qd[0, h, i] @ kd[0, h].T))
+        assert np.abs(P[n] - ref).max() < 1e-15

@@ -6,9 +6,12 @@ a cudaMalloc).  Its scratch is a static device array inside the library.
 Called through the C ABI (ctypes on libfa.so) twice in a row, on different
 inputs so that the second call runs over the first call's leftovers in the
 shared array, and each result is compared with fa_fwd_splitkv given a
-caller-allocated workspace, within the parity tolerances of the other tests.
-This file is collected last so that a run stopping at the first failure has
-run every other test first; it also passes on its own in a fresh process.
+caller-allocated workspace.  Both run the same kernels on the same data with
+only the scratch address differing, so the outputs must be bit-identical (a
+part left stale from the first call would show).  This file is collected last
+so that a run stopping at the first failure has run every other test first; it
+also passes on its own in a fresh process.  The argument checks, which make no
+CUDA call, are compared with fa_fwd_splitkv's on the CPU.
 """
 import ctypes
 
@@ -18,8 +21,6 @@ import torch
 
 from exact_attention_32_gb300 import build as fa_build
 from exact_attention_32_gb300 import make_inputs
-
-pytestmark = pytest.mark.gpu
 
 MAX_O, MEAN_O, MAX_LSE = 2e-2, 2e-3, 1e-3
 LIMIT = 32 * 1024 * 1024  # FA_SPLITKV_NOALLOC_MAX_BYTES
@@ -58,9 +59,10 @@ def run(lib, noalloc, q, k, v, scale, causal, S):
                                 B, H, N, d, scale, int(causal), S, ws.data_ptr(), need, stream)
     assert st == 0, lib.fa_status_string(st)
     assert lib.fa_get_device_status(None) == 0
-    return o.double().cpu().numpy(), lse.double().cpu().numpy()
+    return o.cpu(), lse.cpu()
 
 
+@pytest.mark.gpu
 @pytest.mark.parametrize("B,H,N,d,causal,S", [(2, 4, 1000, 128, True, 3), (1, 8, 700, 64, False, 4)])
 def test_noalloc_matches_workspace_version_twice(lib, B, H, N, d, causal, S):
     assert lib.fa_fwd_splitkv_workspace_bytes(B, H, N, d, S) <= LIMIT
@@ -69,11 +71,32 @@ def test_noalloc_matches_workspace_version_twice(lib, B, H, N, d, causal, S):
         q, k, v = (t.cuda() for t in make_inputs(B, H, N, d, seed=7000 + 10 * call + d, q_gain=1.0 + 3 * call))
         o1, l1 = run(lib, True, q, k, v, scale, causal, S)
         o2, l2 = run(lib, False, q, k, v, scale, causal, S)
-        assert np.isfinite(o1).all() and np.isfinite(l1).all()
-        err, lerr = np.abs(o1 - o2), np.abs(l1 - l2)
-        assert err.max() <= MAX_O and err.mean() <= MEAN_O and lerr.max() <= MAX_LSE
+        assert torch.isfinite(o1.float()).all() and torch.isfinite(l1).all()
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("B,H,N,d,scale,causal,S", [
+    (0, 1, 128, 64, 0.125, 0, 2), (1, 1, 0, 64, 0.125, 0, 2), (1, 1, 128, 96, 0.125, 0, 2),
+    (1, 1, (1 << 31) - 100, 256, 0.125, 0, 2), (1 << 20, 1 << 20, 4, 64, 0.125, 0, 2),
+    (1, 1, 128, 64, 0.0, 0, 2), (1, 1, 128, 64, float("nan"), 0, 2), (1, 1, 128, 64, 0.125, 2, 2),
+    (1, 1, 128, 64, 0.125, 0, 0), (1, 1, 128, 64, 0.125, 0, 33), (1, 2, 128, 96, 0.125, 0, 40)])
+def test_argument_errors_match_the_workspace_version(lib, B, H, N, d, scale, causal, S):
+    # every case fails the size, scale, causal or n_splits rules, which both
+    # entry points check before any CUDA call and in the same order
+    args = (None,) * 5 + (B, H, N, d, scale, causal, S)
+    a = lib.fa_fwd_splitkv_noalloc(*args, None)
+    b = lib.fa_fwd_splitkv(*args, None, 1 << 40, None)
+    assert a == b and a != 0, (a, b)
+
+
+def test_limit_is_checked_before_any_device_call(lib):
+    # a valid problem whose parts exceed the array: refused from the sizes alone
+    B, H, N, d, S = 1, 32, 4096, 128, 4
+    assert lib.fa_fwd_splitkv_workspace_bytes(B, H, N, d, S) > LIMIT
+    assert lib.fa_fwd_splitkv_noalloc(*(None,) * 5, B, H, N, d, 0.125, 0, S, None) == FA_ERR_WORKSPACE_LIMIT
+
+
+@pytest.mark.gpu
 def test_noalloc_refuses_problems_beyond_its_array(lib):
     B, H, N, d, S = 1, 32, 4096, 128, 4
     assert lib.fa_fwd_splitkv_workspace_bytes(B, H, N, d, S) > LIMIT
