@@ -38,8 +38,13 @@
 // Keys >= N and, when causal, keys j > i are set to -inf before the max
 // ("6.1 ...", section 8.3: the K/V out-of-range mask).
 //
-// The epilogue (O / l to bf16, LSE) writes straight from registers to global
-// memory, one row per thread; rows past N are not written.
+// The epilogue (O / l to bf16) goes through shared memory: each softmax warp
+// writes 32-column chunks of its 32 rows there and one thread stores each
+// chunk with a TMA store, so global memory sees whole 64-byte row pieces
+// rather than one 16-byte piece of 32 different rows per instruction; the
+// tensor map clips the rows past N.  LSE is stored directly (a warp's 32 rows
+// are contiguous).  The fp32 partials of a key split and the block-sparse
+// forward store directly from registers.
 //
 // Every mbarrier wait is bounded; a wait that gives up sets FA_ERR_TIMEOUT in
 // a device status word and the CTA winds down (waiting, bounded, for its own
@@ -49,6 +54,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "fa.h"
@@ -93,7 +99,10 @@ struct Cfg {
     static constexpr int kNumBars = 9 + 2 * kStages;
     // block-sparse tile records: one per K/V ring slot, one per query tile
     static constexpr int kMetaOffset = kBarOffset + kNumBars * 8 + 16;
-    static constexpr int kSmemBytes = 1024 + kMetaOffset + (kStages + 2) * 4;
+    // epilogue staging of O (bf16 output): two 32 x 32 chunks (2 KB each) per softmax warp
+    static constexpr int kStageOffset = (kMetaOffset + (kStages + 2) * 4 + 1023) / 1024 * 1024;
+    static constexpr int kStageBytes = 8 * 4096;
+    static constexpr int kSmemBytes = 1024 + kStageOffset + kStageBytes;
     static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
 };
 
@@ -256,7 +265,7 @@ __device__ __forceinline__ bool tile0_skips_last(const Unit &w, int N)
 template <int D, bool CAUSAL, bool OUT_F32, bool FP8, bool SPARSE>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, void *__restrict__ o, float *__restrict__ lse, int N,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, void *__restrict__ o, float *__restrict__ lse, int N,
                  int BH, int n_mblocks, int n_units, int n_splits, int kv_chunk, int hg, float scale, float scale_log2,
                  const float *__restrict__ qs, const float *__restrict__ ks, const float *__restrict__ vs,
                  const uint8_t *__restrict__ bm, int nb)
@@ -461,7 +470,12 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                                 dv_hi, idO, (jj > 1 || kk > 0) ? 1u : 0u);
                             }
                         }
-                        if (t == 0 && skip0 && j == w.n_kv - 1) continue;  // fully masked for query tile 0
+                        if (t == 0 && skip0 && j == w.n_kv - 1) {
+                            // fully masked for query tile 0, whose last P V has just been issued:
+                            // its epilogue need not wait for the rest of the unit
+                            mma_commit(bars.o_full(0));
+                            continue;
+                        }
                         if constexpr (SPARSE)  // this S tile's record, for the softmax (published by the arrive below)
                             s_meta[t] = (meta & (kMetaTile | kMetaLast)) | (((meta >> (30 - t)) & 1u) << 30);
                         const uint32_t aq_lo = dq_lo + t * kTile16;
@@ -497,10 +511,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (!ok) break;
                 mma_commit(bars.q_empty());  // the last reads of this unit's Q are issued
                 for (int t = 0; t < kQTiles && ok; ++t) {
-                    if (t == 0 && skip0) {  // its last P V went out with the unit's last tile
-                        mma_commit(bars.o_full(t));
-                        continue;
-                    }
+                    if (t == 0 && skip0) continue;  // committed with the unit's last tile
                     if (!(ok = mbar_wait(bars.p_full(t), ((t == 0 ? jg0 : jg1) - 1) & 1, kWaitLimitNs))) break;
                     tc_fence_after();
 #pragma unroll
@@ -772,19 +783,15 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             const int64_t out_row = out_row_of();
             const float inv_l = lr > 0.f ? (FP8 ? vs[w.bh] : 1.f) / lr : 0.f;
+            if constexpr (OUT_F32 || SPARSE) {
+                // the fp32 partials of a key split, and the block-sparse forward (whose
+                // registers are at their limit), store straight from registers
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tO + c * 32, r);
-                tmem_wait_ld();
-                if (row_g < N) {
-                    if (OUT_F32) {
-                        float4 *orow = reinterpret_cast<float4 *>(static_cast<float *>(o) + out_row * D + c * 32);
-#pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4)
-                            orow[q4] = make_float4(__uint_as_float(r[q4 * 4 + 0]) * inv_l, __uint_as_float(r[q4 * 4 + 1]) * inv_l,
-                                                   __uint_as_float(r[q4 * 4 + 2]) * inv_l, __uint_as_float(r[q4 * 4 + 3]) * inv_l);
-                    } else {
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tO + c * 32, r);
+                    tmem_wait_ld();
+                    if (row_g < N && SPARSE) {
                         __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(o) + out_row * D + c * 32;
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
@@ -795,6 +802,48 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             v.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * inv_l, __uint_as_float(r[q4 * 8 + 7]) * inv_l);
                             *reinterpret_cast<uint4 *>(orow + q4 * 8) = v;
                         }
+                    } else if (row_g < N) {
+                        float4 *orow = reinterpret_cast<float4 *>(static_cast<float *>(o) + out_row * D + c * 32);
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            orow[q4] = make_float4(__uint_as_float(r[q4 * 4 + 0]) * inv_l, __uint_as_float(r[q4 * 4 + 1]) * inv_l,
+                                                   __uint_as_float(r[q4 * 4 + 2]) * inv_l, __uint_as_float(r[q4 * 4 + 3]) * inv_l);
+                    }
+                }
+            } else {
+                // 32-column chunks through this warp's two 2 KB staging buffers: 32 rows of
+                // 64 bytes in the 64-byte swizzle (16-byte piece q of row r at q ^ ((r >> 1) & 3)),
+                // one TMA store per chunk; a buffer is refilled once the store issued from it
+                // two chunks earlier (or in the previous unit) has been read
+                // (the address is rebuilt here rather than kept live through the softmax loop)
+                const uint32_t stage = ((smem_u32(smem_raw) + 1023u) & ~1023u) + C::kStageOffset + warp * 4096;
+                const int row0 = w.q_row0 + t * kBlockM + (warp & 3) * 32;
+                if (lane == 0) bulk_wait_read0();
+                __syncwarp();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tO + c * 32, r);
+                    tmem_wait_ld();
+                    if (c >= 2) {
+                        if (lane == 0) bulk_wait_read1();
+                        __syncwarp();
+                    }
+                    const uint32_t buf = stage + (c & 1) * 2048 + lane * 64;
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(r[q4 * 8 + 0]) * inv_l, __uint_as_float(r[q4 * 8 + 1]) * inv_l);
+                        v.y = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2]) * inv_l, __uint_as_float(r[q4 * 8 + 3]) * inv_l);
+                        v.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * inv_l, __uint_as_float(r[q4 * 8 + 5]) * inv_l);
+                        v.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * inv_l, __uint_as_float(r[q4 * 8 + 7]) * inv_l);
+                        st_shared_v4(buf + ((q4 ^ ((lane >> 1) & 3)) << 4), v);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && row0 < N) {
+                        tma_store_3d(&tm_o, stage + (c & 1) * 2048, c * 32, row0, w.bh);
+                        bulk_commit();
                     }
                 }
             }
@@ -803,6 +852,384 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             ++uc;
         }
         if (!ok) report_timeout();
+        if (!OUT_F32 && !SPARSE && lane == 0) bulk_wait0();  // every O store of this warp has completed
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------- d = 64 dense forward
+//
+// At d = 64 a tile's MMAs are short against its softmax, and in the forward
+// above each query tile's chain softmax(j) -> P V(j) -> S(j+1) -> softmax(j+1)
+// makes the softmax wait for every S (S_t(j+1) overwrites the P_t(j) that
+// P V(j) reads).  Here tensor memory keeps P apart from S, per query tile t:
+//     S_t [128 t, 128 t + 128), O_t [256 + 64 t, +64), P_t [384 + 64 t, +64)
+// so S_t(j+1) is computed as soon as the softmax has read S_t(j) into its
+// registers (it arrives on s_free[t]), while it is still working on tile j;
+// the softmax then runs from tile to tile without waiting.  Before storing
+// P_t(j) (and before rescaling O_t) the softmax waits for P V_t(j-1), whose
+// commit goes to o_done[t].  The divisor of O is summed as at d = 128 (the
+// rounded terms in heavy tiles; there is no ones column here).  Q is
+// double-buffered, so the next unit's first S can start as soon as both
+// query tiles have issued the current unit's last S.  Per K/V tile the MMA
+// thread issues S_0(j) and S_1(j) (each once its tile's softmax has read the
+// previous S), then the P V of item j - 1 for both tiles (each once its
+// softmax has stored P), and the P V of the unit's last item at its end; a
+// query tile 0 that skips a unit's last tile simply has no S or P V there.
+constexpr int kD64Stages = 6;
+struct D64Cfg {
+    static constexpr int kTileBytes = kBlockN * 128;                  // 128 rows of 64 bf16
+    static constexpr int kRingOffset = 2 * kQTiles * kTileBytes;      // two Q buffers of two tiles
+    static constexpr int kStageOffset = kRingOffset + kD64Stages * kTileBytes;
+    static constexpr int kBarOffset = kStageOffset + 8 * 4096;        // O staging, 4 KB per softmax warp
+    // q_full[2], q_empty[2], s_full[2], s_free[2], p_full[2], o_done[2], mma_done, kv_full[S], kv_empty[S]
+    static constexpr int kNumBars = 13 + 2 * kD64Stages;
+    static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
+    static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
+};
+
+struct D64Bars {
+    uint32_t base;
+    __device__ uint32_t q_full(int b) const { return base + 8u * b; }
+    __device__ uint32_t q_empty(int b) const { return base + 16u + 8u * b; }
+    __device__ uint32_t s_full(int t) const { return base + 32u + 8u * t; }
+    __device__ uint32_t s_free(int t) const { return base + 48u + 8u * t; }
+    __device__ uint32_t p_full(int t) const { return base + 64u + 8u * t; }
+    __device__ uint32_t o_done(int t) const { return base + 80u + 8u * t; }
+    __device__ uint32_t mma_done() const { return base + 96u; }
+    __device__ uint32_t full(int s) const { return base + 104u + 8u * s; }
+    __device__ uint32_t empty(int s) const { return base + 104u + 8u * (kD64Stages + s); }
+};
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+fa_fwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  float *__restrict__ lse, int N, int BH, int n_mblocks, int n_units, int hg, float scale,
+                  float scale_log2)
+{
+    using C = D64Cfg;
+    constexpr int S = kD64Stages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s_base = smem_u32(smem);
+    const D64Bars bars{s_base + C::kBarOffset};
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kBarOffset + C::kNumBars * 8);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool run = *reinterpret_cast<volatile int *>(&g_tc_status) == 0;
+
+    if (tid == 0) {
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bars.q_full(b), 1);
+            mbar_init(bars.q_empty(b), 1);
+            mbar_init(bars.s_full(b), 1);
+            mbar_init(bars.s_free(b), kBlockM / 32);  // one arrive per softmax warp
+            mbar_init(bars.p_full(b), kBlockM / 32);
+            mbar_init(bars.o_done(b), 1);
+        }
+        mbar_init(bars.mma_done(), 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bars.full(s), 1);
+            mbar_init(bars.empty(s), 1);
+        }
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (!run) {
+    } else if (warp == kLoadWarp) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            bool ok = true;
+            int it = 0, uc = 0;
+            for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
+                const Unit w = unit_of<CAUSAL, false, true>(u, N, BH, n_mblocks, 1, N, hg);
+                const int qb = uc & 1;  // Q buffer of this unit: free once unit uc - 2 released it
+                if (!(ok = mbar_wait(bars.q_empty(qb), ((uc >> 1) & 1) ^ 1, kWaitLimitNs))) break;
+                mbar_arrive_expect_tx(bars.q_full(qb), kQTiles * C::kTileBytes);
+                for (int t = 0; t < kQTiles; ++t)
+                    tma_load_3d(s_base + (qb * kQTiles + t) * C::kTileBytes, &tm_q, bars.q_full(qb), 0,
+                                w.q_row0 + t * kBlockM, w.bh);
+                ++uc;
+                for (int j = 0; j < w.n_kv && ok; ++j) {
+                    for (int kind = 0; kind < 2; ++kind, ++it) {
+                        const int slot = it % S, use = it / S;
+                        if (!(ok = mbar_wait(bars.empty(slot), (use & 1) ^ 1, kWaitLimitNs))) break;
+                        mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
+                        tma_load_3d(s_base + C::kRingOffset + slot * C::kTileBytes, kind == 0 ? &tm_k : &tm_v,
+                                    bars.full(slot), 0, j * kBlockN, w.bh);
+                    }
+                }
+            }
+            if (!ok) report_timeout();
+            const uint64_t lim = ok ? kWaitLimitNs : kCleanupLimitNs;
+            for (int k = max(0, uc - 2); k < uc; ++k) mbar_wait(bars.q_full(k & 1), (k >> 1) & 1, lim);
+            for (int k = max(0, it - S); k < it; ++k) mbar_wait(bars.full(k % S), (k / S) & 1, lim);
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(kBlockM, kBlockN, false);
+            constexpr uint32_t idO = idesc_bf16_f32(kBlockM, 64, true);
+            const uint64_t dq0 = smem_desc_sw128(s_base, 16, 1024);
+            const uint64_t dr0 = smem_desc_sw128(s_base + C::kRingOffset, 16, 1024);
+            const uint64_t dv0 = smem_desc_sw128(s_base + C::kRingOffset, kBlockN * 128, 1024);  // V, MN-major
+            const uint32_t dq_lo = static_cast<uint32_t>(dq0), d_hi = static_cast<uint32_t>(dq0 >> 32);
+            const uint32_t dr_lo = static_cast<uint32_t>(dr0), dv_lo = static_cast<uint32_t>(dv0);
+            constexpr uint32_t kTile16 = C::kTileBytes >> 4;
+            bool ok = true;
+            int it = 0, uc = 0;    // ring position of the unit's K_0, units done
+            int gs0 = 0, gs1 = 0;  // S items issued per query tile (all units)
+            int gp0 = 0, gp1 = 0;  // P V items issued per query tile
+            // the item whose P V is still to be issued: its V position, whether it is the
+            // first of its unit, and whether query tile 0 ran it
+            int pend_v = -1;
+            bool pend_first = false, pend0 = false;
+            auto issue_pv = [&](int t, int vpos, bool first) {
+                const uint32_t bv = dv_lo + (vpos % S) * kTile16;
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk)
+                    mma_ts_lohi(tmem + 256 + t * 64, tmem + 384 + t * 64 + kk * 8, bv + kk * 128, d_hi, idO,
+                                (!first || kk > 0) ? 1u : 0u);
+                mma_commit(bars.o_done(t));
+            };
+            // P V of the pending item, for both query tiles (tile 0 only if it ran it)
+            auto flush_pending = [&]() {
+                if (pend_v < 0) return true;
+                if (!mbar_wait(bars.full(pend_v % S), (pend_v / S) & 1, kWaitLimitNs)) return false;
+                if (pend0) {
+                    if (!mbar_wait(bars.p_full(0), gp0 & 1, kWaitLimitNs)) return false;
+                    tc_fence_after();
+                    issue_pv(0, pend_v, pend_first);
+                    ++gp0;
+                }
+                if (!mbar_wait(bars.p_full(1), gp1 & 1, kWaitLimitNs)) return false;
+                tc_fence_after();
+                issue_pv(1, pend_v, pend_first);
+                ++gp1;
+                mma_commit(bars.empty(pend_v % S));  // V read by every P V it feeds
+                pend_v = -1;
+                return true;
+            };
+            auto issue_s = [&](int t, int qb, int pos) {
+                const uint32_t aq = dq_lo + (qb * kQTiles + t) * kTile16;
+                const uint32_t bk = dr_lo + (pos % S) * kTile16;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ss_lohi(tmem + t * 128, aq + 2 * kk, d_hi, bk + 2 * kk, d_hi, idS, kk > 0 ? 1u : 0u);
+                mma_commit(bars.s_full(t));
+            };
+            for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
+                const Unit w = unit_of<CAUSAL, false, true>(u, N, BH, n_mblocks, 1, N, hg);
+                const int n = w.n_kv, n0 = n - (CAUSAL && w.q_row0 + kBlockM < N ? 1 : 0), qb = uc & 1;
+                if (!(ok = mbar_wait(bars.q_full(qb), (uc >> 1) & 1, kWaitLimitNs))) break;
+                for (int j = 0; j < n && ok; ++j) {
+                    const int pos = it + 2 * j;
+                    if (!(ok = mbar_wait(bars.full(pos % S), (pos / S) & 1, kWaitLimitNs))) break;
+                    // S of item j, once each query tile has read its previous S into registers
+                    if (j < n0) {
+                        if (gs0 > 0 && !(ok = mbar_wait(bars.s_free(0), (gs0 - 1) & 1, kWaitLimitNs))) break;
+                        tc_fence_after();
+                        issue_s(0, qb, pos);
+                        ++gs0;
+                    }
+                    if (gs1 > 0 && !(ok = mbar_wait(bars.s_free(1), (gs1 - 1) & 1, kWaitLimitNs))) break;
+                    tc_fence_after();
+                    issue_s(1, qb, pos);
+                    ++gs1;
+                    mma_commit(bars.empty(pos % S));                // K_j read by every S it feeds
+                    if (j == n - 1) mma_commit(bars.q_empty(qb));   // the unit's last reads of its Q
+                    // then the P V of the previous item, while the softmax works on this one
+                    if (!(ok = flush_pending())) break;
+                    pend_v = pos + 1;
+                    pend_first = j == 0;
+                    pend0 = j < n0;
+                }
+                // the unit's last P V now: the epilogue must not wait for the next unit's loads
+                if (ok) ok = flush_pending();
+                it += 2 * n;
+                ++uc;
+            }
+            if (!ok) report_timeout();
+            mma_commit(bars.mma_done());
+            mbar_wait(bars.mma_done(), 0, ok ? kWaitLimitNs : kCleanupLimitNs);
+        }
+    } else {
+        // --------------------------------------------------------------- softmax
+        const int t = warp >> 2;
+        const int row = tid & 127;
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_off + t * 128;
+        const uint32_t tO = tmem + lane_off + 256 + t * 64;
+        const uint32_t tP = tmem + lane_off + 384 + t * 64;
+        const float c_u = scale_log2;
+        bool ok = true;
+        int g = 0;  // tiles processed by this warpgroup (all units): the S, P and P V item index
+        for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
+            const Unit w = unit_of<CAUSAL, false, true>(u, N, BH, n_mblocks, 1, N, hg);
+            const int row_g = w.q_row0 + t * kBlockM + row;
+            const int n_mine = w.n_kv - (t == 0 && CAUSAL && w.q_row0 + kBlockM < N ? 1 : 0);
+            float m_ref = -INFINITY, l = 0.f, lr = 0.f;
+            for (int j = 0; j < n_mine; ++j, ++g) {
+                if (!mbar_wait_warp(bars.s_full(t), g & 1, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float s[kBlockN];
+                {
+                    uint32_t rr[4][32];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, rr[c]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(rr[c][i]);
+                }
+                // S_t is in registers: the next S may overwrite it
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.s_free(t));
+                const int k0 = j * kBlockN;
+                if (k0 + kBlockN > N || (CAUSAL && k0 + kBlockN - 1 > w.q_row0 + t * kBlockM)) {
+                    const int lim = CAUSAL ? min(N - 1, row_g) : N - 1;
+#pragma unroll
+                    for (int i = 0; i < kBlockN; ++i)
+                        if (k0 + i > lim) s[i] = -INFINITY;
+                }
+                float mx[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int b0 = 16 * q;
+                    float a = fmax3(s[b0], s[b0 + 1], s[b0 + 2]);
+#pragma unroll
+                    for (int i = 3; i < 15; i += 2) a = fmax3(a, s[b0 + i], s[b0 + i + 1]);
+                    mx[q] = fmaxf(a, s[b0 + 15]);
+                }
+                const float mt =
+                    fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+                const float m_new = fmaxf(m_ref, mt);
+                const bool need = (m_new - m_ref) * c_u > kRescaleLog2;  // true while m_ref = -inf
+                float alpha = 1.f;
+                if (need) {
+                    alpha = ex2((m_ref - m_new) * c_u);
+                    m_ref = m_new;
+                }
+                const float mc = (m_ref == -INFINITY ? 0.f : m_ref) * c_u;
+                const bool heavy = __any_sync(0xffffffffu, ex2(fmaf(mt, c_u, -mc)) > kHeavyShare * (l * alpha));
+                // P_t and O_t are free once the previous tile's P V has completed
+                if (j > 0) {
+                    if (!mbar_wait_warp(bars.o_done(t), (g - 1) & 1, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                const float2 c2 = make_float2(c_u, c_u), nmc2 = make_float2(-mc, -mc);
+                float2 lf[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                make_float2(0.f, 0.f)};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 x = fma2(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), c2, nmc2);
+                        const float p0 = ex2(x.x), p1 = ex2(x.y);
+                        pk[i] = pack_bf16x2(p0, p1);
+                        lf[c] = add2(lf[c], make_float2(p0, p1));
+                    }
+                    tmem_st16(tP + c * 16, pk);
+                }
+                const float2 lfs = add2(add2(lf[0], lf[1]), add2(lf[2], lf[3]));
+                // the divisor of O: the rounded terms in heavy tiles, the fp32 terms elsewhere
+                // (as in the forward above)
+                float add = lfs.x + lfs.y;
+                if (heavy) {
+                    tmem_wait_st();
+                    float lq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t rr[32];
+                        tmem_ld32(tP + h * 32, rr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) lq[i & 3] = add_bf16x2(lq[i & 3], rr[i]);
+                    }
+                    add = (lq[0] + lq[1]) + (lq[2] + lq[3]);
+                }
+                lr = lr * alpha + add;
+                l = l * alpha + (lfs.x + lfs.y);
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t rr[32];
+                        tmem_ld32(tO + c * 32, rr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const float2 y = mul2(make_float2(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1])),
+                                                  make_float2(alpha, alpha));
+                            rr[i] = __float_as_uint(y.x);
+                            rr[i + 1] = __float_as_uint(y.y);
+                        }
+                        tmem_st32(tO + c * 32, rr);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.p_full(t));
+            }
+            // epilogue once the unit's last P V (item g - 1) has completed
+            if (!ok || !(ok = mbar_wait_warp(bars.o_done(t), (g - 1) & 1, kWaitLimitNs))) break;
+            tc_fence_after();
+            const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
+            const uint32_t stage = s_base + C::kStageOffset + warp * 4096;
+            const int row0 = w.q_row0 + t * kBlockM + (warp & 3) * 32;
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t rr[32];
+                tmem_ld32(tO + c * 32, rr);
+                tmem_wait_ld();
+                const uint32_t buf = stage + c * 2048 + lane * 64;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint4 v;
+                    v.x = pack_bf16x2(__uint_as_float(rr[q4 * 8 + 0]) * inv_l, __uint_as_float(rr[q4 * 8 + 1]) * inv_l);
+                    v.y = pack_bf16x2(__uint_as_float(rr[q4 * 8 + 2]) * inv_l, __uint_as_float(rr[q4 * 8 + 3]) * inv_l);
+                    v.z = pack_bf16x2(__uint_as_float(rr[q4 * 8 + 4]) * inv_l, __uint_as_float(rr[q4 * 8 + 5]) * inv_l);
+                    v.w = pack_bf16x2(__uint_as_float(rr[q4 * 8 + 6]) * inv_l, __uint_as_float(rr[q4 * 8 + 7]) * inv_l);
+                    st_shared_v4(buf + ((q4 ^ ((lane >> 1) & 3)) << 4), v);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && row0 < N) {
+                    tma_store_3d(&tm_o, stage + c * 2048, c * 32, row0, w.bh);
+                    bulk_commit();
+                }
+            }
+            if (row_g < N) lse[static_cast<int64_t>(w.bh) * N + row_g] = l > 0.f ? m_ref * scale + logf(l) : -INFINITY;
+        }
+        if (!ok) report_timeout();
+        if (lane == 0) bulk_wait0();
     }
     tc_fence_before();
     __syncthreads();
@@ -835,6 +1262,21 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
+// bf16 O [BH][N][d] as a 3-D tensor for the epilogue's TMA stores: box = 32
+// columns (64 bytes) x 32 rows x 1 slice, 64-byte swizzle.
+bool make_out_map(CUtensorMap *m, void *base, int64_t BH, int64_t N, int d)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 // [BH][N][d] (bf16, or E4M3 as bytes) viewed as a 3-D tensor (d fastest);
 // box = 128 bytes of columns x 128 rows x 1 slice.
 bool make_map(CUtensorMap *m, const void *base, int64_t BH, int64_t N, int d, int elem = 2)
@@ -857,10 +1299,14 @@ cudaError_t launch(const FaProblem &p, void *o, float *lse, int n_splits, int kv
                    const uint8_t *bm = nullptr)
 {
     using C = Cfg<D, FP8>;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     const int64_t BH = p.B * p.H;
     if (!make_map(&mq, p.q, BH, p.N, D, C::kElem) || !make_map(&mk, p.k, BH, p.N, D, C::kElem) ||
         !make_map(&mv, p.v, BH, p.N, D, C::kElem))
+        return cudaErrorInvalidValue;
+    if (OUT_F32 || SPARSE)
+        mo = mq;  // not used: these variants store O directly
+    else if (!make_out_map(&mo, o, BH, p.N, D))
         return cudaErrorInvalidValue;
     auto kern = fa_fwd_tc_kernel<D, CAUSAL, OUT_F32, FP8, SPARSE>;
     cudaError_t e = set_max_dynamic_smem<fa_fwd_tc_kernel<D, CAUSAL, OUT_F32, FP8, SPARSE>>(C::kSmemBytes);
@@ -881,9 +1327,36 @@ cudaError_t launch(const FaProblem &p, void *o, float *lse, int n_splits, int kv
     }
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
     kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
-        mq, mk, mv, o, lse, static_cast<int>(p.N), static_cast<int>(BH), static_cast<int>(n_mblocks),
+        mq, mk, mv, mo, o, lse, static_cast<int>(p.N), static_cast<int>(BH), static_cast<int>(n_mblocks),
         static_cast<int>(n_units), n_splits, kv_chunk, static_cast<int>(hg), p.scale, scale_log2, qs, ks, vs, bm,
         static_cast<int>((p.N + kBlockN - 1) / kBlockN));
+    return cudaGetLastError();
+}
+
+template <bool CAUSAL>
+cudaError_t launch_d64(const FaProblem &p, cudaStream_t stream)
+{
+    CUtensorMap mq, mk, mv, mo;
+    const int64_t BH = p.B * p.H;
+    if (!make_map(&mq, p.q, BH, p.N, 64) || !make_map(&mk, p.k, BH, p.N, 64) || !make_map(&mv, p.v, BH, p.N, 64) ||
+        !make_out_map(&mo, p.o, BH, p.N, 64))
+        return cudaErrorInvalidValue;
+    cudaError_t e = set_max_dynamic_smem<fa_fwd_d64_kernel<CAUSAL>>(D64Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int64_t n_mblocks = (p.N + kQTiles * kBlockM - 1) / (kQTiles * kBlockM);
+    const int64_t n_units = n_mblocks * BH;
+    if (n_units > 0x7fffffffLL || BH > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const int64_t grid = n_units < p.sm_count ? n_units : p.sm_count;  // persistent: one CTA per SM
+    const int64_t kv_bytes = 2 * p.N * 64 * 2;
+    int64_t hg = BH;
+    if (BH * kv_bytes > (int64_t(160) << 20)) {
+        hg = (int64_t(64) << 20) / kv_bytes;
+        hg = hg < 1 ? 1 : (hg > BH ? BH : hg);
+    }
+    const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
+    fa_fwd_d64_kernel<CAUSAL><<<static_cast<unsigned>(grid), kThreads, D64Cfg::kSmemBytes, stream>>>(
+        mq, mk, mv, mo, p.lse, static_cast<int>(p.N), static_cast<int>(BH), static_cast<int>(n_mblocks),
+        static_cast<int>(n_units), static_cast<int>(hg), p.scale, scale_log2);
     return cudaGetLastError();
 }
 
@@ -901,6 +1374,20 @@ cudaError_t dispatch(const FaProblem &p, void *o, float *lse, int n_splits, int 
 
 cudaError_t fa_launch_tc(const FaProblem &p, cudaStream_t stream)
 {
+    if (p.d == 64) {
+        // The d = 64 kernel (P apart from S, Q double-buffered) wins where units are
+        // short and their start and end weigh; the forward above (ones column, P over
+        // S) wins on long units.  Measured on one GB300: 378 against 332 TFLOP/s at
+        // N = 512 causal, 482 / 467 at N = 1000 causal, 711 / 684 at N = 2048 causal,
+        // 833 / 840 at N = 4096 causal, 907 / 955 at N = 16384 causal; non-causal
+        // 683 / 618 at N = 512, equal at N = 1000, 861 / 869 at N = 2048.  The
+        // switch is at a mean of 9 K/V tiles per 256-row unit.
+        const int64_t nt = (p.N + kBlockN - 1) / kBlockN;
+        const int64_t n_mblocks = (p.N + kQTiles * kBlockM - 1) / (kQTiles * kBlockM);
+        int64_t tiles = 0;
+        for (int64_t mb = 0; mb < n_mblocks; ++mb) tiles += p.causal ? std::min(nt, 2 * (mb + 1)) : nt;
+        if (tiles <= 9 * n_mblocks) return p.causal ? launch_d64<true>(p, stream) : launch_d64<false>(p, stream);
+    }
     return dispatch<false>(p, p.o, p.lse, 1, static_cast<int>(p.N), stream);
 }
 
