@@ -46,6 +46,10 @@
 // are contiguous).  The fp32 partials of a key split and the block-sparse
 // forward store directly from registers.
 //
+// The kernels in this file: fa_fwd_tc_kernel (above; bf16, d = 64 and 128, with
+// the key-split and block-sparse variants) and fa_fwd_dp_kernel (below; P kept
+// apart from S: bf16 at d = 64 for short units, and the E4M3 forward).
+//
 // Every mbarrier wait is bounded; a wait that gives up sets FA_ERR_TIMEOUT in
 // a device status word and the CTA winds down (waiting, bounded, for its own
 // copies and MMAs in flight, then freeing its tensor memory).
@@ -78,20 +82,20 @@ constexpr uint64_t kCleanupLimitNs = 20000000ull;    // 20 ms per wait while win
 
 __device__ int g_tc_status;  // sticky FA_ERR_TIMEOUT, read and cleared by fa_get_device_status
 
-template <int D, bool FP8>
+template <int D>
 struct Cfg {
-    static constexpr int kElem = FP8 ? 1 : 2;               // bytes per element (E4M3 or bf16)
+    static constexpr int kElem = 2;                         // bytes per element (bf16)
     static constexpr int kRowBytes = D * kElem;
     static constexpr int kTileBytes = kBlockN * kRowBytes;  // one Q, K or V tile
     static constexpr int kAtoms = kRowBytes / 128;          // 128-byte-wide column blocks per tile
     static constexpr int kStages = kTileBytes == 32768 ? 4 : 8;  // K/V ring slots
     static constexpr int kSSteps = kRowBytes / 32;          // S MMA K steps (32 bytes of each row)
-    static constexpr int kPVKeys = FP8 ? 32 : 16;           // keys per P V MMA
+    static constexpr int kPVKeys = 16;                      // keys per P V MMA
     static constexpr int kPVSteps = kBlockN / kPVKeys;
-    // d = 64 (bf16): the P V MMA runs at N = 80.  B's extra 16 columns come from a
+    // d = 64: the P V MMA runs at N = 80.  B's extra 16 columns come from a
     // constant block (a column of ones, then zeros), so column 64 of O accumulates
     // the row sum of exactly the bf16 P that the MMA multiplies, rescaled with O.
-    static constexpr bool kOnesCol = (D == 64 && !FP8);
+    static constexpr bool kOnesCol = (D == 64);
     static constexpr int kPVN = kOnesCol ? 80 : D;             // N of the P V MMA
     static constexpr int kOnesOffset = (kQTiles + kStages) * kTileBytes;
     static constexpr int kBarOffset = kOnesOffset + (kOnesCol ? kBlockN * 128 : 0);
@@ -245,32 +249,27 @@ __device__ __forceinline__ Unit unit_of(int u, int N, int BH, int n_mblocks, int
 
 // Causal, all keys in one launch: a unit's last K/V tile starts at or past row
 // q_row0 + 128 whenever query tile 1 has rows (q_row0 + 128 < N), so it is
-// fully masked for query tile 0, which then skips it (its S, P and P V).  (The
-// E4M3 softmax keeps the plain loop: its registers are at the limit.)
-template <bool CAUSAL, bool SPLIT, bool SPARSE, bool FP8>
+// fully masked for query tile 0, which then skips it (its S, P and P V).
+template <bool CAUSAL, bool SPLIT, bool SPARSE>
 __device__ __forceinline__ bool tile0_skips_last(const Unit &w, int N)
 {
-    return CAUSAL && !SPLIT && !SPARSE && !FP8 && w.q_row0 + kBlockM < N;
+    return CAUSAL && !SPLIT && !SPARSE && w.q_row0 + kBlockM < N;
 }
 
 // OUT_F32: O is written as fp32 (the partial results of a key split) instead
 // of bf16; split s writes its rows at o + s * B*H*N*d and lse + s * B*H*N.
-// FP8: Q, K, V are E4M3 with one fp32 scale per (b, h) each (qs, ks, vs): the
-// S MMAs see the raw E4M3 values and the scales are folded into the exponent
-// constant and the LSE; P is rounded to E4M3 for a kind::f8f6f4 P V MMA and vs
-// is applied in the epilogue.
 // SPARSE: bm is a [nb][nb] 0/1 block mask (nb = ceil(N/128)) over (query block,
 // key block); K/V tiles no query block of the unit admits are skipped, and a
 // tile is fully masked for a query tile whose block does not admit it.
-template <int D, bool CAUSAL, bool OUT_F32, bool FP8, bool SPARSE>
+template <int D, bool CAUSAL, bool OUT_F32, bool SPARSE>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, void *__restrict__ o, float *__restrict__ lse, int N,
-                 int BH, int n_mblocks, int n_units, int n_splits, int kv_chunk, int hg, float scale, float scale_log2,
-                 const float *__restrict__ qs, const float *__restrict__ ks, const float *__restrict__ vs,
-                 const uint8_t *__restrict__ bm, int nb)
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                 void *__restrict__ o, float *__restrict__ lse, int N, int BH, int n_mblocks, int n_units,
+                 int n_splits, int kv_chunk, int hg, float scale, float scale_log2, const uint8_t *__restrict__ bm,
+                 int nb)
 {
-    using C = Cfg<D, FP8>;
+    using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s_base = smem_u32(smem);
@@ -420,10 +419,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------- MMA issue
         if (lane == 0) {
-            constexpr uint32_t idS = FP8 ? idesc_e4m3_f32(kBlockM, kBlockN, false)
-                                         : idesc_bf16_f32(kBlockM, kBlockN, false);
-            constexpr uint32_t idO =
-                FP8 ? idesc_e4m3_f32(kBlockM, D, true) : idesc_bf16_f32(kBlockM, C::kPVN, true);
+            constexpr uint32_t idS = idesc_bf16_f32(kBlockM, kBlockN, false);
+            constexpr uint32_t idO = idesc_bf16_f32(kBlockM, C::kPVN, true);
             // descriptors are built once; a K step only moves the start address
             // (low 32 bits, in 16-byte units): +32 bytes inside a 128-byte-wide
             // column block, +16 KB to the next block (S), +2 KB per 16 keys (P V)
@@ -444,7 +441,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 uint32_t prev_v_lo = 0;
                 int prev_v = -1;
                 int jj = 0;  // K/V tiles of this unit processed so far
-                const bool skip0 = tile0_skips_last<CAUSAL, OUT_F32, SPARSE, FP8>(w, N);
+                const bool skip0 = tile0_skips_last<CAUSAL, OUT_F32, SPARSE>(w, N);
                 // (block-sparse: the producer's records give the live tiles; j only counts)
                 for (int j = 0; j < w.n_kv && ok; ++j) {
                     const int kslot = it % C::kStages, kuse = it / C::kStages;
@@ -462,12 +459,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                             for (int kk = 0; kk < C::kPVSteps; ++kk) {
                                 const uint32_t boff = (kk * C::kPVKeys * 128) >> 4;
-                                if constexpr (FP8)
-                                    mma_ts_f8_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + boff,
-                                                   dv_hi, idO, (jj > 1 || kk > 0) ? 1u : 0u);
-                                else
-                                    mma_ts_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + boff,
-                                                dv_hi, idO, (jj > 1 || kk > 0) ? 1u : 0u);
+                                mma_ts_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + boff, dv_hi,
+                                            idO, (jj > 1 || kk > 0) ? 1u : 0u);
                             }
                         }
                         if (t == 0 && skip0 && j == w.n_kv - 1) {
@@ -482,12 +475,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                         for (int kk = 0; kk < C::kSSteps; ++kk) {
                             const uint32_t koff = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
-                            if constexpr (FP8)
-                                mma_ss_f8_lohi(tmem + t * 128, aq_lo + koff, dq_hi, dk_lo + koff, dk_hi, idS,
-                                               kk > 0 ? 1u : 0u);
-                            else
-                                mma_ss_lohi(tmem + t * 128, aq_lo + koff, dq_hi, dk_lo + koff, dk_hi, idS,
-                                            kk > 0 ? 1u : 0u);
+                            mma_ss_lohi(tmem + t * 128, aq_lo + koff, dq_hi, dk_lo + koff, dk_hi, idS,
+                                        kk > 0 ? 1u : 0u);
                         }
                         mma_commit(bars.s_full(t));
                         if constexpr (SPARSE) mbar_arrive(bars.s_full(t));
@@ -517,12 +506,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                     for (int kk = 0; kk < C::kPVSteps; ++kk) {
                         const uint32_t boff = (kk * C::kPVKeys * 128) >> 4;
-                        if constexpr (FP8)
-                            mma_ts_f8_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + boff, dv_hi,
-                                           idO, (jj > 1 || kk > 0) ? 1u : 0u);
-                        else
-                            mma_ts_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + boff, dv_hi, idO,
-                                        (jj > 1 || kk > 0) ? 1u : 0u);
+                        mma_ts_lohi(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, prev_v_lo + boff, dv_hi, idO,
+                                    (jj > 1 || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(bars.o_full(t));
                 }
@@ -580,15 +565,14 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 continue;
             }
-            // exponent constant and LSE scale of this slice (E4M3 scales folded in)
-            const float c_u = FP8 ? scale_log2 * qs[w.bh] * ks[w.bh] : scale_log2;
+            const float c_u = scale_log2;
             float m_ref = -INFINITY;  // reference max, unscaled units
             float l = 0.f;            // exp-sum relative to m_ref (fp32 terms; gives LSE)
             float lr = 0.f;           // the divisor of O (see the row sums below)
             int jj = 0;  // K/V tiles of this unit processed so far
             // block-sparse: the loop counts the unit's live tiles; each one's index and
             // admission bit come with its S tile (the MMA thread's record)
-            const int n_mine = w.n_kv - (t == 0 && tile0_skips_last<CAUSAL, OUT_F32, SPARSE, FP8>(w, N) ? 1 : 0);
+            const int n_mine = w.n_kv - (t == 0 && tile0_skips_last<CAUSAL, OUT_F32, SPARSE>(w, N) ? 1 : 0);
             for (int jc = 0; jc < n_mine; ++jc) {
                 if (!mbar_wait_warp(bars.s_full(t), jg & 1, kWaitLimitNs)) {
                     ok = false;
@@ -646,7 +630,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const float mc = (m_ref == -INFINITY ? 0.f : m_ref) * c_u;
                 // how the divisor of O is summed at d = 128 (see the row sums below): every
                 // term inline in the key-split forward, else per tile as needed
-                constexpr bool kInlineSum = !FP8 && !C::kOnesCol && OUT_F32;
+                constexpr bool kInlineSum = !C::kOnesCol && OUT_F32;
                 constexpr bool kHeavyTiles = !C::kOnesCol && !OUT_F32;
                 bool heavy = false;
                 if constexpr (kHeavyTiles)
@@ -655,80 +639,50 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 float2 lf[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                 make_float2(0.f, 0.f)};
                 float lq[4] = {0.f, 0.f, 0.f, 0.f};
-                if constexpr (FP8) {
-                    // P rounded to E4M3, four per tensor-memory column (128 keys -> 32 columns)
-                    uint32_t pw[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float2 x01 = fma2(make_float2(s[4 * i], s[4 * i + 1]), c2, nmc2);
-                        const float2 x23 = fma2(make_float2(s[4 * i + 2], s[4 * i + 3]), c2, nmc2);
-                        const float p0 = ex2(x01.x), p1 = ex2(x01.y), p2 = ex2(x23.x), p3 = ex2(x23.y);
-                        lf[i & 3] = add2(lf[i & 3], add2(make_float2(p0, p1), make_float2(p2, p3)));
-                        pw[i] = pack_e4m3x4(p0, p1, p2, p3);
-                    }
-                    uint32_t h0[16], h1[16];
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t p[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        h0[i] = pw[i];
-                        h1[i] = pw[16 + i];
-                    }
-                    tmem_st16(tS, h0);
-                    tmem_st16(tS + 16, h1);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t p[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float2 x = fma2(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), c2, nmc2);
-                            const float p0 = ex2(x.x), p1 = ex2(x.y);
-                            p[i] = pack_bf16x2(p0, p1);
-                            if constexpr (kInlineSum) {
-                                lf[i & 3] = add2(lf[i & 3], make_float2(p0, p1));
-                                lq[i & 3] = add_bf16x2(lq[i & 3], p[i]);
-                            } else {
-                                lf[c] = add2(lf[c], make_float2(p0, p1));  // one partial per chunk
-                            }
+                        const float2 x = fma2(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), c2, nmc2);
+                        const float p0 = ex2(x.x), p1 = ex2(x.y);
+                        p[i] = pack_bf16x2(p0, p1);
+                        if constexpr (kInlineSum) {
+                            lf[i & 3] = add2(lf[i & 3], make_float2(p0, p1));
+                            lq[i & 3] = add_bf16x2(lq[i & 3], p[i]);
+                        } else {
+                            lf[c] = add2(lf[c], make_float2(p0, p1));  // one partial per chunk
                         }
-                        tmem_st16(tS + c * 16, p);
                     }
+                    tmem_st16(tS + c * 16, p);
                 }
                 const float2 lf01 = add2(lf[0], lf[1]), lf23 = add2(lf[2], lf[3]);
                 const float2 lfs = add2(lf01, lf23);
                 if constexpr (kInlineSum) {
                     lr = lr * alpha + ((lq[0] + lq[1]) + (lq[2] + lq[3]));
                 } else if constexpr (kHeavyTiles) {
-                    // d = 128 (bf16 or E4M3 P): O is divided by lr, which must be the sum of
-                    // the rounded P the MMA sees wherever few keys carry a row (a mismatch
-                    // of the rounding step on a top weight shows in O: 2^-9 for bf16, 2^-4
-                    // for E4M3), while over many comparable keys the fp32 sum's
-                    // rounding differences average out.  So the exact rounded sum is
-                    // taken only in "heavy" tiles, where for some row of the warp the
-                    // tile's largest P exceeds kHeavyShare of the row's running sum
-                    // (always the unit's first tile): P is read back from tensor memory
-                    // and summed exactly (mixed-precision adds; E4M3 decoded through f16).  Any key whose final weight
+                    // d = 128: O is divided by lr, which must be the sum of the rounded P the
+                    // MMA sees wherever few keys carry a row (a mismatch of the rounding step
+                    // on a top weight shows in O: 2^-9), while over many comparable keys the
+                    // fp32 sum's rounding differences average out.  So the exact rounded sum
+                    // is taken only in "heavy" tiles, where for some row of the warp the
+                    // tile's largest P exceeds kHeavyShare of the row's running sum (always
+                    // the unit's first tile): P is read back from tensor memory and summed
+                    // exactly (mixed-precision adds).  Any key whose final weight
                     // exceeds kHeavyShare lies in a heavy tile.  Light tiles add their fp32
                     // sum.  (d = 64 gets the rounded sum from the MMA, column 64 of O; the
                     // key-split forward, whose variants run out of registers with this
                     // branch, sums every rounded term inline.)
                     float add = lfs.x + lfs.y;
-                    if (heavy) {
+                    if (heavy) {  // 64 columns of two bf16 each
                         tmem_wait_st();
-                        if constexpr (FP8) {  // 32 columns of four E4M3 each
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
                             uint32_t r[32];
-                            tmem_ld32(tS, r);
+                            tmem_ld32(tS + h * 32, r);
                             tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) lq[i & 3] = add_e4m3x4(lq[i & 3], r[i]);
-                        } else {  // 64 columns of two bf16 each
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                uint32_t r[32];
-                                tmem_ld32(tS + h * 32, r);
-                                tmem_wait_ld();
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) lq[i & 3] = add_bf16x2(lq[i & 3], r[i]);
-                            }
+                            for (int i = 0; i < 32; ++i) lq[i & 3] = add_bf16x2(lq[i & 3], r[i]);
                         }
                         add = (lq[0] + lq[1]) + (lq[2] + lq[3]);
                     }
@@ -782,7 +736,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tmem_wait_ld();
             }
             const int64_t out_row = out_row_of();
-            const float inv_l = lr > 0.f ? (FP8 ? vs[w.bh] : 1.f) / lr : 0.f;
+            const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
             if constexpr (OUT_F32 || SPARSE) {
                 // the fp32 partials of a key split, and the block-sparse forward (whose
                 // registers are at their limit), store straight from registers
@@ -847,8 +801,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                 }
             }
-            const float scale_u = FP8 ? scale * qs[w.bh] * ks[w.bh] : scale;
-            if (row_g < N) lse[out_row] = l > 0.f ? m_ref * scale_u + logf(l) : -INFINITY;
+            if (row_g < N) lse[out_row] = l > 0.f ? m_ref * scale + logf(l) : -INFINITY;
             ++uc;
         }
         if (!ok) report_timeout();
@@ -862,19 +815,25 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
 }
 
-// ------------------------------------------------------- d = 64 dense forward
+// ------------------------------------------------ forward with P apart from S
 //
-// At d = 64 a tile's MMAs are short against its softmax, and in the forward
-// above each query tile's chain softmax(j) -> P V(j) -> S(j+1) -> softmax(j+1)
-// makes the softmax wait for every S (S_t(j+1) overwrites the P_t(j) that
-// P V(j) reads).  Here tensor memory keeps P apart from S, per query tile t:
-//     S_t [128 t, 128 t + 128), O_t [256 + 64 t, +64), P_t [384 + 64 t, +64)
-// so S_t(j+1) is computed as soon as the softmax has read S_t(j) into its
-// registers (it arrives on s_free[t]), while it is still working on tile j;
-// the softmax then runs from tile to tile without waiting.  Before storing
-// P_t(j) (and before rescaling O_t) the softmax waits for P V_t(j-1), whose
-// commit goes to o_done[t].  The divisor of O is summed as at d = 128 (the
-// rounded terms in heavy tiles; there is no ones column here).  Q is
+// In the forward above each query tile's chain softmax(j) -> P V(j) -> S(j+1)
+// -> softmax(j+1) makes the softmax wait for every S (S_t(j+1) overwrites the
+// P_t(j) that P V(j) reads).  Where memory allows, this kernel keeps P apart:
+//   bf16, d = 64:   tensor memory per query tile t holds S_t [128 t, +128),
+//                   O_t [256 + 64 t, +64) and P_t [384 + 64 t, +64), and
+//                   P V is a TS MMA (A = P from tensor memory);
+//   E4M3, d = 128:  S_t [128 t, +128), O_t [256 + 128 t, +128) fill tensor
+//                   memory, so P_t (16 KB of E4M3) goes to shared memory in
+//                   the 128-byte swizzle and P V is an SS MMA.
+// Rows of 128 bytes (64 bf16 or 128 E4M3) make the Q, K, V and P tiles of both
+// variants 16 KB with the same K steps of 32 bytes.  S_t(j+1) is computed as
+// soon as the softmax has read S_t(j) into its registers (it arrives on
+// s_free[t]), while it is still working on tile j; the softmax then runs from
+// tile to tile without waiting.  Before storing P_t(j) (and before rescaling
+// O_t) the softmax waits for P V_t(j-1), whose commit goes to o_done[t].  The
+// divisor of O is summed as in the forward above (the rounded terms in heavy
+// tiles; there is no ones column here).  Q is
 // double-buffered, so the next unit's first S can start as soon as both
 // query tiles have issued the current unit's last S.  Per K/V tile the MMA
 // thread issues S_0(j) and S_1(j) (each once its tile's softmax has read the
@@ -882,14 +841,18 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 // softmax has stored P), and the P V of the unit's last item at its end; a
 // query tile 0 that skips a unit's last tile simply has no S or P V there.
 constexpr int kD64Stages = 6;
+template <bool FP8>
 struct D64Cfg {
-    static constexpr int kTileBytes = kBlockN * 128;                  // 128 rows of 64 bf16
+    static constexpr int kD = FP8 ? 128 : 64;                         // head dimension
+    static constexpr int kTileBytes = kBlockN * 128;                  // 128 rows of 128 bytes
     static constexpr int kRingOffset = 2 * kQTiles * kTileBytes;      // two Q buffers of two tiles
-    static constexpr int kStageOffset = kRingOffset + kD64Stages * kTileBytes;
+    static constexpr int kPOffset = kRingOffset + kD64Stages * kTileBytes;  // E4M3: P_0, P_1
+    static constexpr int kStageOffset = kPOffset + (FP8 ? kQTiles * kTileBytes : 0);
     static constexpr int kBarOffset = kStageOffset + 8 * 4096;        // O staging, 4 KB per softmax warp
     // q_full[2], q_empty[2], s_full[2], s_free[2], p_full[2], o_done[2], mma_done, kv_full[S], kv_empty[S]
     static constexpr int kNumBars = 13 + 2 * kD64Stages;
     static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
+    static constexpr int kOCol = 256;                                 // O_t at kOCol + t * kD
     static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
 };
 
@@ -906,14 +869,16 @@ struct D64Bars {
     __device__ uint32_t empty(int s) const { return base + 104u + 8u * (kD64Stages + s); }
 };
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
-fa_fwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                  float *__restrict__ lse, int N, int BH, int n_mblocks, int n_units, int hg, float scale,
-                  float scale_log2)
+fa_fwd_dp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                 float *__restrict__ lse, int N, int BH, int n_mblocks, int n_units, int hg, float scale,
+                 float scale_log2, const float *__restrict__ qs, const float *__restrict__ ks,
+                 const float *__restrict__ vs)
 {
-    using C = D64Cfg;
+    using C = D64Cfg<FP8>;
+    constexpr int D = C::kD;
     constexpr int S = kD64Stages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -984,8 +949,8 @@ fa_fwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------- MMA issue
         if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(kBlockM, kBlockN, false);
-            constexpr uint32_t idO = idesc_bf16_f32(kBlockM, 64, true);
+            constexpr uint32_t idS = FP8 ? idesc_e4m3_f32(kBlockM, kBlockN, false) : idesc_bf16_f32(kBlockM, kBlockN, false);
+            constexpr uint32_t idO = FP8 ? idesc_e4m3_f32(kBlockM, D, true) : idesc_bf16_f32(kBlockM, D, true);
             const uint64_t dq0 = smem_desc_sw128(s_base, 16, 1024);
             const uint64_t dr0 = smem_desc_sw128(s_base + C::kRingOffset, 16, 1024);
             const uint64_t dv0 = smem_desc_sw128(s_base + C::kRingOffset, kBlockN * 128, 1024);  // V, MN-major
@@ -1002,10 +967,18 @@ fa_fwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             bool pend_first = false, pend0 = false;
             auto issue_pv = [&](int t, int vpos, bool first) {
                 const uint32_t bv = dv_lo + (vpos % S) * kTile16;
+                if constexpr (FP8) {  // A = P_t from shared memory, 32 keys (32 bytes) per K step
+                    const uint32_t ap = dq_lo + ((C::kPOffset + t * C::kTileBytes) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk)
-                    mma_ts_lohi(tmem + 256 + t * 64, tmem + 384 + t * 64 + kk * 8, bv + kk * 128, d_hi, idO,
-                                (!first || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kBlockN / 32; ++kk)
+                        mma_ss_f8_lohi(tmem + C::kOCol + t * D, ap + 2 * kk, d_hi, bv + kk * 256, d_hi, idO,
+                                       (!first || kk > 0) ? 1u : 0u);
+                } else {  // A = P_t from tensor memory, 16 keys (8 columns) per K step
+#pragma unroll
+                    for (int kk = 0; kk < kBlockN / 16; ++kk)
+                        mma_ts_lohi(tmem + C::kOCol + t * D, tmem + 384 + t * 64 + kk * 8, bv + kk * 128, d_hi, idO,
+                                    (!first || kk > 0) ? 1u : 0u);
+                }
                 mma_commit(bars.o_done(t));
             };
             // P V of the pending item, for both query tiles (tile 0 only if it ran it)
@@ -1030,8 +1003,12 @@ fa_fwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 const uint32_t aq = dq_lo + (qb * kQTiles + t) * kTile16;
                 const uint32_t bk = dr_lo + (pos % S) * kTile16;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ss_lohi(tmem + t * 128, aq + 2 * kk, d_hi, bk + 2 * kk, d_hi, idS, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < 4; ++kk) {  // 32 bytes of each 128-byte row per K step
+                    if constexpr (FP8)
+                        mma_ss_f8_lohi(tmem + t * 128, aq + 2 * kk, d_hi, bk + 2 * kk, d_hi, idS, kk > 0 ? 1u : 0u);
+                    else
+                        mma_ss_lohi(tmem + t * 128, aq + 2 * kk, d_hi, bk + 2 * kk, d_hi, idS, kk > 0 ? 1u : 0u);
+                }
                 mma_commit(bars.s_full(t));
             };
             for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
@@ -1075,13 +1052,16 @@ fa_fwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int row = tid & 127;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_off + t * 128;
-        const uint32_t tO = tmem + lane_off + 256 + t * 64;
-        const uint32_t tP = tmem + lane_off + 384 + t * 64;
-        const float c_u = scale_log2;
+        const uint32_t tO = tmem + lane_off + C::kOCol + t * D;
+        const uint32_t tP = tmem + lane_off + 384 + t * 64;  // bf16 only
+        // E4M3: this thread's row of P_t in shared memory (128 bytes, 16-byte pieces swizzled)
+        const uint32_t sP = s_base + C::kPOffset + t * C::kTileBytes + row * 128;
         bool ok = true;
         int g = 0;  // tiles processed by this warpgroup (all units): the S, P and P V item index
         for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
             const Unit w = unit_of<CAUSAL, false, true>(u, N, BH, n_mblocks, 1, N, hg);
+            // exponent constant of this slice (E4M3 scales folded in)
+            const float c_u = FP8 ? scale_log2 * qs[w.bh] * ks[w.bh] : scale_log2;
             const int row_g = w.q_row0 + t * kBlockM + row;
             const int n_mine = w.n_kv - (t == 0 && CAUSAL && w.q_row0 + kBlockM < N ? 1 : 0);
             float m_ref = -INFINITY, l = 0.f, lr = 0.f;
@@ -1144,40 +1124,66 @@ fa_fwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 const float2 c2 = make_float2(c_u, c_u), nmc2 = make_float2(-mc, -mc);
                 float2 lf[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                 make_float2(0.f, 0.f)};
+                float add;  // the divisor of O: the rounded terms in heavy tiles, the fp32 terms elsewhere
+                if constexpr (FP8) {
+                    // P rounded to E4M3, four per word, 16-byte pieces into this row of P_t
+                    uint32_t pw[32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float2 x = fma2(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), c2, nmc2);
-                        const float p0 = ex2(x.x), p1 = ex2(x.y);
-                        pk[i] = pack_bf16x2(p0, p1);
-                        lf[c] = add2(lf[c], make_float2(p0, p1));
+                    for (int i = 0; i < 32; ++i) {
+                        const float2 x01 = fma2(make_float2(s[4 * i], s[4 * i + 1]), c2, nmc2);
+                        const float2 x23 = fma2(make_float2(s[4 * i + 2], s[4 * i + 3]), c2, nmc2);
+                        const float p0 = ex2(x01.x), p1 = ex2(x01.y), p2 = ex2(x23.x), p3 = ex2(x23.y);
+                        lf[i & 3] = add2(lf[i & 3], add2(make_float2(p0, p1), make_float2(p2, p3)));
+                        pw[i] = pack_e4m3x4(p0, p1, p2, p3);
                     }
-                    tmem_st16(tP + c * 16, pk);
-                }
-                const float2 lfs = add2(add2(lf[0], lf[1]), add2(lf[2], lf[3]));
-                // the divisor of O: the rounded terms in heavy tiles, the fp32 terms elsewhere
-                // (as in the forward above)
-                float add = lfs.x + lfs.y;
-                if (heavy) {
-                    tmem_wait_st();
-                    float lq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t rr[32];
-                        tmem_ld32(tP + h * 32, rr);
-                        tmem_wait_ld();
+                    for (int q4 = 0; q4 < 8; ++q4)
+                        st_shared_v4(sP + ((q4 ^ (row & 7)) << 4),
+                                     make_uint4(pw[4 * q4], pw[4 * q4 + 1], pw[4 * q4 + 2], pw[4 * q4 + 3]));
+                    fence_proxy_async_smem();  // visible to the P V MMA
+                    const float2 lfs = add2(add2(lf[0], lf[1]), add2(lf[2], lf[3]));
+                    add = lfs.x + lfs.y;
+                    if (heavy) {  // the rounded terms, from the packed words still in registers
+                        float lq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) lq[i & 3] = add_bf16x2(lq[i & 3], rr[i]);
+                        for (int i = 0; i < 32; ++i) lq[i & 3] = add_e4m3x4(lq[i & 3], pw[i]);
+                        add = (lq[0] + lq[1]) + (lq[2] + lq[3]);
                     }
-                    add = (lq[0] + lq[1]) + (lq[2] + lq[3]);
+                    l = l * alpha + (lfs.x + lfs.y);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float2 x = fma2(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), c2, nmc2);
+                            const float p0 = ex2(x.x), p1 = ex2(x.y);
+                            pk[i] = pack_bf16x2(p0, p1);
+                            lf[c] = add2(lf[c], make_float2(p0, p1));
+                        }
+                        tmem_st16(tP + c * 16, pk);
+                    }
+                    const float2 lfs = add2(add2(lf[0], lf[1]), add2(lf[2], lf[3]));
+                    add = lfs.x + lfs.y;
+                    if (heavy) {
+                        tmem_wait_st();
+                        float lq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t rr[32];
+                            tmem_ld32(tP + h * 32, rr);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) lq[i & 3] = add_bf16x2(lq[i & 3], rr[i]);
+                        }
+                        add = (lq[0] + lq[1]) + (lq[2] + lq[3]);
+                    }
+                    l = l * alpha + (lfs.x + lfs.y);
                 }
                 lr = lr * alpha + add;
-                l = l * alpha + (lfs.x + lfs.y);
                 if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
+                    for (int c = 0; c < D / 32; ++c) {
                         uint32_t rr[32];
                         tmem_ld32(tO + c * 32, rr);
                         tmem_wait_ld();
@@ -1199,17 +1205,22 @@ fa_fwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             // epilogue once the unit's last P V (item g - 1) has completed
             if (!ok || !(ok = mbar_wait_warp(bars.o_done(t), (g - 1) & 1, kWaitLimitNs))) break;
             tc_fence_after();
-            const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
+            const float inv_l = lr > 0.f ? (FP8 ? vs[w.bh] : 1.f) / lr : 0.f;
             const uint32_t stage = s_base + C::kStageOffset + warp * 4096;
             const int row0 = w.q_row0 + t * kBlockM + (warp & 3) * 32;
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
+            // O in 32-column chunks through two 2 KB buffers (as in the forward above)
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < D / 32; ++c) {
                 uint32_t rr[32];
                 tmem_ld32(tO + c * 32, rr);
                 tmem_wait_ld();
-                const uint32_t buf = stage + c * 2048 + lane * 64;
+                if (c >= 2) {
+                    if (lane == 0) bulk_wait_read1();
+                    __syncwarp();
+                }
+                const uint32_t buf = stage + (c & 1) * 2048 + lane * 64;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     uint4 v;
@@ -1222,11 +1233,12 @@ fa_fwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0 && row0 < N) {
-                    tma_store_3d(&tm_o, stage + c * 2048, c * 32, row0, w.bh);
+                    tma_store_3d(&tm_o, stage + (c & 1) * 2048, c * 32, row0, w.bh);
                     bulk_commit();
                 }
             }
-            if (row_g < N) lse[static_cast<int64_t>(w.bh) * N + row_g] = l > 0.f ? m_ref * scale + logf(l) : -INFINITY;
+            const float scale_u = FP8 ? scale * qs[w.bh] * ks[w.bh] : scale;
+            if (row_g < N) lse[static_cast<int64_t>(w.bh) * N + row_g] = l > 0.f ? m_ref * scale_u + logf(l) : -INFINITY;
         }
         if (!ok) report_timeout();
         if (lane == 0) bulk_wait0();
@@ -1293,12 +1305,11 @@ bool make_map(CUtensorMap *m, const void *base, int64_t BH, int64_t N, int d, in
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool CAUSAL, bool OUT_F32, bool FP8 = false, bool SPARSE = false>
+template <int D, bool CAUSAL, bool OUT_F32, bool SPARSE = false>
 cudaError_t launch(const FaProblem &p, void *o, float *lse, int n_splits, int kv_chunk, cudaStream_t stream,
-                   const float *qs = nullptr, const float *ks = nullptr, const float *vs = nullptr,
                    const uint8_t *bm = nullptr)
 {
-    using C = Cfg<D, FP8>;
+    using C = Cfg<D>;
     CUtensorMap mq, mk, mv, mo;
     const int64_t BH = p.B * p.H;
     if (!make_map(&mq, p.q, BH, p.N, D, C::kElem) || !make_map(&mk, p.k, BH, p.N, D, C::kElem) ||
@@ -1308,8 +1319,8 @@ cudaError_t launch(const FaProblem &p, void *o, float *lse, int n_splits, int kv
         mo = mq;  // not used: these variants store O directly
     else if (!make_out_map(&mo, o, BH, p.N, D))
         return cudaErrorInvalidValue;
-    auto kern = fa_fwd_tc_kernel<D, CAUSAL, OUT_F32, FP8, SPARSE>;
-    cudaError_t e = set_max_dynamic_smem<fa_fwd_tc_kernel<D, CAUSAL, OUT_F32, FP8, SPARSE>>(C::kSmemBytes);
+    auto kern = fa_fwd_tc_kernel<D, CAUSAL, OUT_F32, SPARSE>;
+    cudaError_t e = set_max_dynamic_smem<fa_fwd_tc_kernel<D, CAUSAL, OUT_F32, SPARSE>>(C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t n_mblocks = (p.N + kQTiles * kBlockM - 1) / (kQTiles * kBlockM);
     const int64_t n_units = n_mblocks * BH * n_splits;
@@ -1328,35 +1339,38 @@ cudaError_t launch(const FaProblem &p, void *o, float *lse, int n_splits, int kv
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
     kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
         mq, mk, mv, mo, o, lse, static_cast<int>(p.N), static_cast<int>(BH), static_cast<int>(n_mblocks),
-        static_cast<int>(n_units), n_splits, kv_chunk, static_cast<int>(hg), p.scale, scale_log2, qs, ks, vs, bm,
+        static_cast<int>(n_units), n_splits, kv_chunk, static_cast<int>(hg), p.scale, scale_log2, bm,
         static_cast<int>((p.N + kBlockN - 1) / kBlockN));
     return cudaGetLastError();
 }
 
-template <bool CAUSAL>
-cudaError_t launch_d64(const FaProblem &p, cudaStream_t stream)
+template <bool CAUSAL, bool FP8>
+cudaError_t launch_dp(const FaProblem &p, cudaStream_t stream, const float *qs = nullptr, const float *ks = nullptr,
+                      const float *vs = nullptr)
 {
+    using C = D64Cfg<FP8>;
     CUtensorMap mq, mk, mv, mo;
     const int64_t BH = p.B * p.H;
-    if (!make_map(&mq, p.q, BH, p.N, 64) || !make_map(&mk, p.k, BH, p.N, 64) || !make_map(&mv, p.v, BH, p.N, 64) ||
-        !make_out_map(&mo, p.o, BH, p.N, 64))
+    const int elem = FP8 ? 1 : 2;
+    if (!make_map(&mq, p.q, BH, p.N, C::kD, elem) || !make_map(&mk, p.k, BH, p.N, C::kD, elem) ||
+        !make_map(&mv, p.v, BH, p.N, C::kD, elem) || !make_out_map(&mo, p.o, BH, p.N, C::kD))
         return cudaErrorInvalidValue;
-    cudaError_t e = set_max_dynamic_smem<fa_fwd_d64_kernel<CAUSAL>>(D64Cfg::kSmemBytes);
+    cudaError_t e = set_max_dynamic_smem<fa_fwd_dp_kernel<CAUSAL, FP8>>(C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t n_mblocks = (p.N + kQTiles * kBlockM - 1) / (kQTiles * kBlockM);
     const int64_t n_units = n_mblocks * BH;
     if (n_units > 0x7fffffffLL || BH > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int64_t grid = n_units < p.sm_count ? n_units : p.sm_count;  // persistent: one CTA per SM
-    const int64_t kv_bytes = 2 * p.N * 64 * 2;
+    const int64_t kv_bytes = 2 * p.N * C::kTileBytes / kBlockN;  // K and V of one slice
     int64_t hg = BH;
     if (BH * kv_bytes > (int64_t(160) << 20)) {
         hg = (int64_t(64) << 20) / kv_bytes;
         hg = hg < 1 ? 1 : (hg > BH ? BH : hg);
     }
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
-    fa_fwd_d64_kernel<CAUSAL><<<static_cast<unsigned>(grid), kThreads, D64Cfg::kSmemBytes, stream>>>(
+    fa_fwd_dp_kernel<CAUSAL, FP8><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
         mq, mk, mv, mo, p.lse, static_cast<int>(p.N), static_cast<int>(BH), static_cast<int>(n_mblocks),
-        static_cast<int>(n_units), static_cast<int>(hg), p.scale, scale_log2);
+        static_cast<int>(n_units), static_cast<int>(hg), p.scale, scale_log2, qs, ks, vs);
     return cudaGetLastError();
 }
 
@@ -1386,7 +1400,8 @@ cudaError_t fa_launch_tc(const FaProblem &p, cudaStream_t stream)
         const int64_t n_mblocks = (p.N + kQTiles * kBlockM - 1) / (kQTiles * kBlockM);
         int64_t tiles = 0;
         for (int64_t mb = 0; mb < n_mblocks; ++mb) tiles += p.causal ? std::min(nt, 2 * (mb + 1)) : nt;
-        if (tiles <= 9 * n_mblocks) return p.causal ? launch_d64<true>(p, stream) : launch_d64<false>(p, stream);
+        if (tiles <= 9 * n_mblocks)
+            return p.causal ? launch_dp<true, false>(p, stream) : launch_dp<false, false>(p, stream);
     }
     return dispatch<false>(p, p.o, p.lse, 1, static_cast<int>(p.N), stream);
 }
@@ -1401,22 +1416,17 @@ cudaError_t fa_launch_tc_sparse(const FaProblem &p, const uint8_t *block_mask, c
 {
     const int N = static_cast<int>(p.N);
     if (p.d == 64)
-        return p.causal ? launch<64, true, false, false, true>(p, p.o, p.lse, 1, N, stream, nullptr, nullptr, nullptr,
-                                                                 block_mask)
-                        : launch<64, false, false, false, true>(p, p.o, p.lse, 1, N, stream, nullptr, nullptr,
-                                                                  nullptr, block_mask);
-    return p.causal ? launch<128, true, false, false, true>(p, p.o, p.lse, 1, N, stream, nullptr, nullptr, nullptr,
-                                                              block_mask)
-                    : launch<128, false, false, false, true>(p, p.o, p.lse, 1, N, stream, nullptr, nullptr, nullptr,
-                                                               block_mask);
+        return p.causal ? launch<64, true, false, true>(p, p.o, p.lse, 1, N, stream, block_mask)
+                        : launch<64, false, false, true>(p, p.o, p.lse, 1, N, stream, block_mask);
+    return p.causal ? launch<128, true, false, true>(p, p.o, p.lse, 1, N, stream, block_mask)
+                    : launch<128, false, false, true>(p, p.o, p.lse, 1, N, stream, block_mask);
 }
 
 cudaError_t fa_launch_tc_fp8(const FaProblem &p, const float *qs, const float *ks, const float *vs,
                              cudaStream_t stream)
 {
     if (p.d != 128) return cudaErrorInvalidValue;
-    return p.causal ? launch<128, true, false, true>(p, p.o, p.lse, 1, static_cast<int>(p.N), stream, qs, ks, vs)
-                    : launch<128, false, false, true>(p, p.o, p.lse, 1, static_cast<int>(p.N), stream, qs, ks, vs);
+    return p.causal ? launch_dp<true, true>(p, stream, qs, ks, vs) : launch_dp<false, true>(p, stream, qs, ks, vs);
 }
 
 int fa_tc_take_status(cudaStream_t stream)
