@@ -196,8 +196,10 @@ __device__ __forceinline__ uint2 mask_row_words(const uint8_t *__restrict__ bm, 
 // Block-sparse tile record, published by the producer for every live K/V tile
 // (per K ring slot) and forwarded by the MMA thread with every S tile: the
 // tile index (bits 0-23), admitted by query tile 0 / 1 (bits 30 / 29), last
-// live tile of the unit (bit 31).
+// live tile of the unit (bit 31).  A unit with no live tile sends one record,
+// kMetaEmptyUnit (no tile has index 2^24 - 1).
 constexpr uint32_t kMetaTile = 0xffffffu, kMetaOwn0 = 1u << 30, kMetaOwn1 = 1u << 29, kMetaLast = 1u << 31;
+constexpr uint32_t kMetaEmptyUnit = kMetaTile | kMetaLast;
 
 __device__ __forceinline__ int unit_index(int r)
 {
@@ -283,23 +285,10 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     const Bars<C::kStages> bars{bar0};
     // K/V tiles a unit processes: all of its range, or in block-sparse mode those
-    // the mask admits for either query block of the unit.  The producer finds
-    // them (32 tiles per mask read) and publishes a record per live tile, which
-    // the MMA thread and the softmax warps follow; any_live (the same mask rows)
-    // tells every role which units have no live tile at all.
-    auto unit_word = [&](const Unit &w, int c) {
-        const int qa = w.q_row0 / kBlockM, qb = qa + 1 < nb ? qa + 1 : qa;
-        return mask_word(bm, nb, qa, qb, w.j0, c, w.n_kv);
-    };
-    auto any_live = [&](const Unit &w) {
-        if constexpr (SPARSE) {
-            for (int c = 0; c < w.n_kv; c += 32)
-                if (unit_word(w, c) != 0) return true;
-            return false;
-        } else {
-            return w.n_kv > 0;
-        }
-    };
+    // the mask admits for either query block of the unit.  Only the producer
+    // reads the mask (32 tiles per read): it publishes a record per live tile,
+    // or one empty-unit record for a unit with none, which the MMA thread and
+    // the softmax warps follow.
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // after a timeout anywhere (sticky until read by the host) CTAs do no work
     const bool run = *reinterpret_cast<volatile int *>(&g_tc_status) == 0;
@@ -351,28 +340,17 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             int it = 0, uc = 0;
             for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
                 const Unit w = unit_of<CAUSAL, OUT_F32, !SPARSE>(u, N, BH, n_mblocks, n_splits, kv_chunk, hg);
-                if (!any_live(w)) continue;  // no admitted key: nothing to load
-                // the Q buffers are free once the previous unit's last S MMAs have completed
-                if (!mbar_wait(bars.q_empty(), (uc & 1) ^ 1, kWaitLimitNs)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(bars.q_full(), kQTiles * C::kTileBytes);
-                for (int t = 0; t < kQTiles; ++t)
-                    for (int a = 0; a < C::kAtoms; ++a)
-                        tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &tm_q, bars.q_full(), a * (128 / C::kElem),
-                                    w.q_row0 + t * kBlockM, w.bh);
-                ++uc;
+                if (!SPARSE && w.n_kv <= 0) continue;  // a key split with no admitted key: nothing to load
                 // block-sparse: the live tiles in order, each published in its K slot's record
                 // with its admission bits and a last-tile flag (found by looking one live
                 // tile ahead); wa / wb are the admission bits of the two query blocks for the
                 // 32-tile group `grp`
+                const int qa = w.q_row0 / kBlockM;
                 uint32_t wa = 0, wb = 0;
                 int grp = -1;
                 auto next_live = [&](int from) {  // the first live tile >= from, or -1
                     for (int c = from & ~31; c < w.n_kv; c += 32) {
                         if ((c >> 5) != grp) {
-                            const int qa = w.q_row0 / kBlockM;
                             const uint2 wab = mask_row_words(bm, nb, qa, qa + 1 < nb ? qa + 1 : qa, w.j0, c, w.n_kv);
                             wa = wab.x;
                             wb = qa + 1 < nb ? wab.y : 0u;  // a second query block past the last row admits nothing
@@ -384,6 +362,27 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     return -1;
                 };
                 int j_live = SPARSE ? next_live(0) : 0;
+                if (SPARSE && j_live < 0) {
+                    // no admitted tile: one record through the K ring tells the MMA thread and the
+                    // softmax warps (no Q, K or V is loaded)
+                    const int slot = it % C::kStages, use = it / C::kStages;
+                    if (!(ok = mbar_wait(bars.empty(slot), (use & 1) ^ 1, kWaitLimitNs))) break;
+                    kv_meta[slot] = kMetaEmptyUnit;
+                    mbar_arrive(bars.full(slot));  // released by this arrive
+                    ++it;
+                    continue;
+                }
+                // the Q buffers are free once the previous unit's last S MMAs have completed
+                if (!mbar_wait(bars.q_empty(), (uc & 1) ^ 1, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(bars.q_full(), kQTiles * C::kTileBytes);
+                for (int t = 0; t < kQTiles; ++t)
+                    for (int a = 0; a < C::kAtoms; ++a)
+                        tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &tm_q, bars.q_full(), a * (128 / C::kElem),
+                                    w.q_row0 + t * kBlockM, w.bh);
+                ++uc;
                 for (int j = 0; j < w.n_kv && ok; ++j) {
                     uint32_t meta = 0;
                     if constexpr (SPARSE) {
@@ -432,16 +431,49 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             constexpr uint32_t kTile16 = C::kTileBytes >> 4;
             bool ok = true;
             int it = 0, uc = 0;     // ring position, units done
-            int jg0 = 0, jg1 = 0;   // S tiles issued for query tile 0 / 1 (all units)
+            int jg0 = 0, jg1 = 0;   // items (S tiles, empty-unit records) sent to query tile 0 / 1 (all units)
+            // block-sparse: an empty-unit record not yet acknowledged (on p_full) by the softmax
+            // of query tile 0 / 1; its s_meta may not be written again before that
+            bool tok0 = false, tok1 = false;
+            auto ack_token = [&](int t) {
+                bool &tk = t ? tok1 : tok0;
+                if (!tk) return true;
+                tk = false;
+                return mbar_wait(bars.p_full(t), ((t ? jg1 : jg0) - 1) & 1, kWaitLimitNs);
+            };
             for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
                 const Unit w = unit_of<CAUSAL, OUT_F32, !SPARSE>(u, N, BH, n_mblocks, n_splits, kv_chunk, hg);
-                if (!any_live(w)) continue;
+                if (!SPARSE && w.n_kv <= 0) continue;  // a key split with no admitted key
+                if constexpr (SPARSE) {
+                    // a unit with no live tile: its one record goes to both softmax warpgroups
+                    const int kslot = it % C::kStages, kuse = it / C::kStages;
+                    if (!(ok = mbar_wait(bars.full(kslot), kuse & 1, kWaitLimitNs))) break;
+                    if (kv_meta[kslot] == kMetaEmptyUnit) {
+                        for (int t = 0; t < kQTiles && ok; ++t) {
+                            if (!(ok = ack_token(t))) break;
+                            s_meta[t] = kMetaEmptyUnit;
+                            mma_commit(bars.s_full(t));
+                            mbar_arrive(bars.s_full(t));
+                            if (t) {
+                                ++jg1;
+                                tok1 = true;
+                            } else {
+                                ++jg0;
+                                tok0 = true;
+                            }
+                        }
+                        mma_commit(bars.empty(kslot));
+                        ++it;
+                        continue;
+                    }
+                }
                 if (!(ok = mbar_wait(bars.q_full(), uc & 1, kWaitLimitNs))) break;
                 tc_fence_after();
                 uint32_t prev_v_lo = 0;
                 int prev_v = -1;
                 int jj = 0;  // K/V tiles of this unit processed so far
                 const bool skip0 = tile0_skips_last<CAUSAL, OUT_F32, SPARSE>(w, N);
+                bool skipped0 = false;  // query tile 0 skipped the unit's last tile
                 // (block-sparse: the producer's records give the live tiles; j only counts)
                 for (int j = 0; j < w.n_kv && ok; ++j) {
                     const int kslot = it % C::kStages, kuse = it / C::kStages;
@@ -463,14 +495,18 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                             idO, (jj > 1 || kk > 0) ? 1u : 0u);
                             }
                         }
+                        // causal: the unit's last tile is fully masked for query tile 0 whenever tile 1
+                        // has rows; tile 0's last P V has just been issued, so its epilogue need not
+                        // wait for the rest of the unit
                         if (t == 0 && skip0 && j == w.n_kv - 1) {
-                            // fully masked for query tile 0, whose last P V has just been issued:
-                            // its epilogue need not wait for the rest of the unit
                             mma_commit(bars.o_full(0));
+                            skipped0 = true;
                             continue;
                         }
-                        if constexpr (SPARSE)  // this S tile's record, for the softmax (published by the arrive below)
+                        if constexpr (SPARSE) {  // this S tile's record, for the softmax (published by the arrive below)
+                            if (jj == 0 && !(ok = ack_token(t))) break;
                             s_meta[t] = (meta & (kMetaTile | kMetaLast)) | (((meta >> (30 - t)) & 1u) << 30);
+                        }
                         const uint32_t aq_lo = dq_lo + t * kTile16;
 #pragma unroll
                         for (int kk = 0; kk < C::kSSteps; ++kk) {
@@ -500,7 +536,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (!ok) break;
                 mma_commit(bars.q_empty());  // the last reads of this unit's Q are issued
                 for (int t = 0; t < kQTiles && ok; ++t) {
-                    if (t == 0 && skip0) continue;  // committed with the unit's last tile
+                    if (t == 0 && skipped0) continue;  // committed with the unit's last tile
                     if (!(ok = mbar_wait(bars.p_full(t), ((t == 0 ? jg0 : jg1) - 1) & 1, kWaitLimitNs))) break;
                     tc_fence_after();
 #pragma unroll
@@ -533,23 +569,23 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int row_g = w.q_row0 + t * kBlockM + row;
             auto out_row_of = [&]() { return (static_cast<int64_t>(w.split) * BH + w.bh) * N + row_g; };
             const bool qb_ok = !SPARSE || (w.q_row0 / kBlockM + t < nb);
-            // block-sparse: the tiles j .. j+31 of the unit that either query block admits
-            // (one lane per tile), to find units with no admitted tile
-            auto load_words = [&](int j) -> uint32_t {
-                const int qa = w.q_row0 / kBlockM, qb2 = qa + 1 < nb ? qa + 1 : qa;
-                const bool in = j + lane < w.n_kv;
-                const int64_t kj = w.j0 + j + lane;
-                const uint8_t a = in ? __ldg(bm + qa * static_cast<int64_t>(nb) + kj) : 0;
-                const uint8_t b = in ? __ldg(bm + qb2 * static_cast<int64_t>(nb) + kj) : 0;
-                return __ballot_sync(0xffffffffu, (a | b) != 0);
-            };
+            // a unit with no admitted key in its split (or, block-sparse, in its mask rows: the
+            // MMA thread's empty-unit record, acknowledged on p_full): O = 0, LSE = -inf (no
+            // weight when merged)
             bool unit_live = w.n_kv > 0;
             if constexpr (SPARSE) {
-                unit_live = false;
-                for (int c = 0; c < w.n_kv && !unit_live; c += 32) unit_live = load_words(c) != 0;
+                if (!mbar_wait_warp(bars.s_full(t), jg & 1, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                unit_live = s_meta[t] != kMetaEmptyUnit;  // the first tile's record, or the empty-unit one
+                if (!unit_live) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars.p_full(t));
+                    ++jg;
+                }
             }
             if (!unit_live) {
-                // no admitted key in this split (or block mask): O = 0, LSE = -inf (no weight when merged)
                 if (row_g < N) {
                     const int64_t out_row = out_row_of();
                     if (OUT_F32) {
