@@ -403,7 +403,7 @@ extern "C" int fa_fwd_fp8(const void *q, const void *k, const void *v, const flo
     p.scale = scale;
     p.causal = causal;
     p.sm_count = sm_count;
-    if (fa_launch_tc_fp8(p, q_scale, k_scale, v_scale, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (fa_launch_fp8(p, q_scale, k_scale, v_scale, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return FA_ERR_LAUNCH;
     return FA_OK;
 }
@@ -468,8 +468,9 @@ extern "C" int fa_get_device_status(void *stream)
         return FA_ERR_LAUNCH;
     }
     const int fwd = fa_tc_take_status(static_cast<cudaStream_t>(stream));
+    const int dp = fa_dp_take_status(static_cast<cudaStream_t>(stream));
     const int bwd = fa_bwd_take_status(static_cast<cudaStream_t>(stream));
-    return fwd != FA_OK ? fwd : bwd;
+    return fwd != FA_OK ? fwd : (dp != FA_OK ? dp : bwd);
 }
 
 extern "C" const char *fa_status_string(int status)

@@ -51,9 +51,14 @@ cudaError_t fa_launch_tc_partials(const FaProblem &p, float *o_parts, float *lse
                                   cudaStream_t stream);
 // The same kernel restricted by a [ceil(N/128)]^2 0/1 block mask over (query block, key block).
 cudaError_t fa_launch_tc_sparse(const FaProblem &p, const uint8_t *block_mask, cudaStream_t stream);
-// The same kernel on E4M3 Q, K, V (d = 128) with per-(b, h) fp32 scales qs, ks, vs.
-cudaError_t fa_launch_tc_fp8(const FaProblem &p, const float *qs, const float *ks, const float *vs,
-                             cudaStream_t stream);
+// The kernel with P apart from S (fa_fwd_dp.cu): bf16 at d = 64 (taken by
+// fa_launch_tc for short units), and E4M3 Q, K, V at d = 128 with per-(b, h)
+// fp32 scales qs, ks, vs.
+cudaError_t fa_launch_dp(const FaProblem &p, cudaStream_t stream);
+cudaError_t fa_launch_fp8(const FaProblem &p, const float *qs, const float *ks, const float *vs,
+                          cudaStream_t stream);
+// Read and clear that kernel's sticky device status (synchronises `stream`).
+int fa_dp_take_status(cudaStream_t stream);
 // Merge of n_parts partial (O fp32, LSE) results of `rows` rows into bf16 O and LSE.
 cudaError_t fa_launch_combine(const float *o_parts, const float *lse_parts, int n_parts, int64_t rows, int d,
                               void *o, float *lse, int sm_count, cudaStream_t stream);
