@@ -23,7 +23,7 @@ _lock = threading.Lock()
 FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_NO_DEVICE",
                 4: "FA_ERR_ARCH", 5: "FA_ERR_LAUNCH", 6: "FA_ERR_TIMEOUT", 7: "FA_ERR_WORKSPACE_LIMIT"}
-EXPORTED = ("fa_fwd", "fa_bh_partition", "fa_fwd_slab", "fa_fwd_host", "fa_fwd_mma", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_combine",
+EXPORTED = ("fa_fwd", "fa_fwd_kernel", "fa_bh_partition", "fa_fwd_slab", "fa_fwd_host", "fa_fwd_mma", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_combine",
             "fa_fwd_splitkv_noalloc", "fa_fwd_fp8", "fa_fwd_blocksparse", "fa_bwd", "fa_bwd_workspace_bytes", "fa_get_device_status",
             "fa_status_string", "fa_version")
 
@@ -47,6 +47,8 @@ def lib():
             L.fa_fwd.restype = ctypes.c_int
             L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
                                  ctypes.c_int, vp]
+            L.fa_fwd_kernel.restype = ctypes.c_int
+            L.fa_fwd_kernel.argtypes = [i64, i64, i64, i64, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
             L.fa_bh_partition.restype = ctypes.c_int
             L.fa_bh_partition.argtypes = [i64, i64, i64, ctypes.POINTER(i64), ctypes.POINTER(i64)]
             L.fa_fwd_slab.restype = ctypes.c_int
@@ -88,6 +90,19 @@ def lib():
 def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
     """Raw call: pointers as ints, ``stream`` a cudaStream_t as int (0 = legacy default)."""
     return lib().fa_fwd(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), int(causal), stream)
+
+
+FWD_KERNEL_NAMES = {0: "fa_fwd_tc_kernel", 1: "fa_fwd_dp_kernel"}
+
+
+def fa_fwd_kernel(B: int, H: int, N: int, d: int, causal: bool) -> str:
+    """Name of the kernel fa_fwd launches for these sizes (pure host
+    computation in the library).  Raises FAError on invalid sizes."""
+    kid = ctypes.c_int(-1)
+    st = lib().fa_fwd_kernel(int(B), int(H), int(N), int(d), int(bool(causal)), ctypes.byref(kid))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_kernel")
+    return FWD_KERNEL_NAMES[kid.value]
 
 
 def fa_bh_partition(n_slices: int, world: int, rank: int):

@@ -158,6 +158,15 @@ extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, floa
     return validate_and_launch(fa_launch_tc, q, k, v, o, lse, B, H, N, d, scale, causal, stream);
 }
 
+extern "C" int fa_fwd_kernel(int64_t B, int64_t H, int64_t N, int64_t d, int causal, int *kernel)
+{
+    const int st = fa_check_sizes(B, H, N, d);
+    if (st != FA_OK) return st;
+    if ((causal != 0 && causal != 1) || kernel == nullptr) return FA_ERR_INVALID_ARG;
+    *kernel = fa_fwd_takes_dp(N, d, causal) ? FA_FWD_KERNEL_DP : FA_FWD_KERNEL_TC;
+    return FA_OK;
+}
+
 extern "C" int fa_bh_partition(int64_t n_slices, int64_t world, int64_t rank, int64_t *begin, int64_t *count)
 {
     if (n_slices < 0 || world < 1 || rank < 0 || rank >= world || begin == nullptr || count == nullptr)

@@ -825,23 +825,26 @@ cudaError_t dispatch(const FaProblem &p, void *o, float *lse, int n_splits, int 
 
 }  // namespace
 
+bool fa_fwd_takes_dp(int64_t N, int64_t d, int causal)
+{
+    if (d != 64) return false;
+    // The d = 64 kernel (P apart from S, Q double-buffered) wins where units are
+    // short and their start and end weigh; the forward above (ones column, P over
+    // S) wins on long units.  Measured on one GB300: 378 against 332 TFLOP/s at
+    // N = 512 causal, 482 / 467 at N = 1000 causal, 711 / 684 at N = 2048 causal,
+    // 833 / 840 at N = 4096 causal, 907 / 955 at N = 16384 causal; non-causal
+    // 683 / 618 at N = 512, equal at N = 1000, 861 / 869 at N = 2048.  The
+    // switch is at a mean of 9 K/V tiles per 256-row unit.
+    const int64_t nt = (N + kBlockN - 1) / kBlockN;
+    const int64_t n_mblocks = (N + kQTiles * kBlockM - 1) / (kQTiles * kBlockM);
+    int64_t tiles = 0;
+    for (int64_t mb = 0; mb < n_mblocks; ++mb) tiles += causal ? std::min(nt, 2 * (mb + 1)) : nt;
+    return tiles <= 9 * n_mblocks;
+}
+
 cudaError_t fa_launch_tc(const FaProblem &p, cudaStream_t stream)
 {
-    if (p.d == 64) {
-        // The d = 64 kernel (P apart from S, Q double-buffered) wins where units are
-        // short and their start and end weigh; the forward above (ones column, P over
-        // S) wins on long units.  Measured on one GB300: 378 against 332 TFLOP/s at
-        // N = 512 causal, 482 / 467 at N = 1000 causal, 711 / 684 at N = 2048 causal,
-        // 833 / 840 at N = 4096 causal, 907 / 955 at N = 16384 causal; non-causal
-        // 683 / 618 at N = 512, equal at N = 1000, 861 / 869 at N = 2048.  The
-        // switch is at a mean of 9 K/V tiles per 256-row unit.
-        const int64_t nt = (p.N + kBlockN - 1) / kBlockN;
-        const int64_t n_mblocks = (p.N + kQTiles * kBlockM - 1) / (kQTiles * kBlockM);
-        int64_t tiles = 0;
-        for (int64_t mb = 0; mb < n_mblocks; ++mb) tiles += p.causal ? std::min(nt, 2 * (mb + 1)) : nt;
-        if (tiles <= 9 * n_mblocks)
-            return fa_launch_dp(p, stream);
-    }
+    if (fa_fwd_takes_dp(p.N, p.d, p.causal)) return fa_launch_dp(p, stream);
     return dispatch<false>(p, p.o, p.lse, 1, static_cast<int>(p.N), stream);
 }
 

@@ -44,7 +44,9 @@ struct FaProblem {
 };
 
 // tcgen05 kernel (TMA, tensor memory, warp-specialised): 256 query rows per CTA.
+// At d = 64 it hands problems of short units to fa_launch_dp (fa_fwd_takes_dp).
 cudaError_t fa_launch_tc(const FaProblem &p, cudaStream_t stream);
+bool fa_fwd_takes_dp(int64_t N, int64_t d, int causal);
 // The same kernel over n_splits key ranges of kv_chunk keys (a multiple of
 // 128): split s writes fp32 O to o_parts + s*B*H*N*d and LSE to lse_parts + s*B*H*N.
 cudaError_t fa_launch_tc_partials(const FaProblem &p, float *o_parts, float *lse_parts, int n_splits, int kv_chunk,

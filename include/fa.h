@@ -81,6 +81,22 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            void *stream);
 
 /*
+ * fa_fwd_kernel - which kernel a call of fa_fwd with these sizes launches.
+ * Both compute the same forward; at d = 64 problems whose work units (256
+ * query rows each) see at most 9 key/value tiles of 128 keys on average go to
+ * the kernel that keeps P apart from S, the rest to the main kernel.  Meant
+ * for profilers and benchmarks that attribute time to a kernel by name.
+ *
+ *   B, H, N, d, causal : as for fa_fwd
+ *   kernel : host output, FA_FWD_KERNEL_TC (fa_fwd_tc_kernel) or
+ *            FA_FWD_KERNEL_DP (fa_fwd_dp_kernel)
+ * Pure host computation.  Returns FA_OK, or fa_fwd's status for invalid sizes
+ * or causal flag, or FA_ERR_INVALID_ARG for a null `kernel` (nothing written).
+ */
+enum fa_fwd_kernel_id { FA_FWD_KERNEL_TC = 0, FA_FWD_KERNEL_DP = 1 };
+int fa_fwd_kernel(int64_t B, int64_t H, int64_t N, int64_t d, int causal, int *kernel);
+
+/*
  * fa_bh_partition - the (b, h) slices one GPU of a sharded problem takes.
  * The programs over (b, h) slices are independent and exchange nothing
  * ("6.1 FlashAttention V1 in detail", section 8.2, the parallel partition),

@@ -94,3 +94,29 @@ def test_host_entry_rejects_bad_arguments_before_any_device_call(libfa, kw):
 
 def test_host_entry_unsupported_head_dim(libfa):
     assert _call_host(libfa, d=96) == 2  # FA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("N,d,causal,expected", [
+    (256, 64, 0, "fa_fwd_dp_kernel"), (1000, 64, 1, "fa_fwd_dp_kernel"), (1000, 64, 0, "fa_fwd_dp_kernel"),
+    (2048, 64, 1, "fa_fwd_dp_kernel"), (2048, 64, 0, "fa_fwd_tc_kernel"), (4096, 64, 1, "fa_fwd_tc_kernel"),
+    (16384, 64, 1, "fa_fwd_tc_kernel"), (256, 128, 0, "fa_fwd_tc_kernel"), (16384, 128, 1, "fa_fwd_tc_kernel")])
+def test_forward_kernel_choice(N, d, causal, expected):
+    # d = 64 problems whose 256-row units see at most 9 key tiles of 128 on
+    # average run on the kernel with P apart from S; all others on the main one
+    import exact_attention_32_gb300 as fa
+    assert fa.fa_fwd_kernel(2, 3, N, d, causal) == expected
+    n_t, n_mb = -(-N // 128), -(-N // 256)
+    tiles = sum(min(n_t, 2 * (mb + 1)) if causal else n_t for mb in range(n_mb))
+    assert (expected == "fa_fwd_dp_kernel") == (d == 64 and tiles <= 9 * n_mb)
+
+
+def test_forward_kernel_choice_rejects_bad_arguments(libfa):
+    f = libfa.fa_fwd_kernel
+    i64 = ctypes.c_int64
+    f.argtypes = [i64, i64, i64, i64, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+    f.restype = ctypes.c_int
+    out = ctypes.c_int(-7)
+    assert f(1, 1, 0, 64, 0, ctypes.byref(out)) == 1 and out.value == -7
+    assert f(1, 1, 128, 96, 0, ctypes.byref(out)) == 2 and out.value == -7
+    assert f(1, 1, 128, 64, 2, ctypes.byref(out)) == 1 and out.value == -7
+    assert f(1, 1, 128, 64, 0, None) == 1
