@@ -694,26 +694,14 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             const int64_t out_row = out_row_of();
             const float inv_l = lr > 0.f ? 1.f / lr : 0.f;
-            if constexpr (OUT_F32 || SPARSE) {
-                // the fp32 partials of a key split, and the block-sparse forward (whose
-                // registers are at their limit), store straight from registers
+            if constexpr (OUT_F32) {
+                // the fp32 partials of a key split store straight from registers
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld32(tO + c * 32, r);
                     tmem_wait_ld();
-                    if (row_g < N && SPARSE) {
-                        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(o) + out_row * D + c * 32;
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint4 v;
-                            v.x = pack_bf16x2(__uint_as_float(r[q4 * 8 + 0]) * inv_l, __uint_as_float(r[q4 * 8 + 1]) * inv_l);
-                            v.y = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2]) * inv_l, __uint_as_float(r[q4 * 8 + 3]) * inv_l);
-                            v.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * inv_l, __uint_as_float(r[q4 * 8 + 5]) * inv_l);
-                            v.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * inv_l, __uint_as_float(r[q4 * 8 + 7]) * inv_l);
-                            *reinterpret_cast<uint4 *>(orow + q4 * 8) = v;
-                        }
-                    } else if (row_g < N) {
+                    if (row_g < N) {
                         float4 *orow = reinterpret_cast<float4 *>(static_cast<float *>(o) + out_row * D + c * 32);
 #pragma unroll
                         for (int q4 = 0; q4 < 8; ++q4)
@@ -762,7 +750,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             ++uc;
         }
         if (!ok) report_timeout();
-        if (!OUT_F32 && !SPARSE && lane == 0) bulk_wait0();  // every O store of this warp has completed
+        if (!OUT_F32 && lane == 0) bulk_wait0();  // every O store of this warp has completed
     }
     tc_fence_before();
     __syncthreads();
@@ -784,8 +772,8 @@ cudaError_t launch(const FaProblem &p, void *o, float *lse, int n_splits, int kv
     if (!make_map(&mq, p.q, BH, p.N, D, C::kElem) || !make_map(&mk, p.k, BH, p.N, D, C::kElem) ||
         !make_map(&mv, p.v, BH, p.N, D, C::kElem))
         return cudaErrorInvalidValue;
-    if (OUT_F32 || SPARSE)
-        mo = mq;  // not used: these variants store O directly
+    if (OUT_F32)
+        mo = mq;  // not used: the key-split partials store O directly
     else if (!make_out_map(&mo, o, BH, p.N, D))
         return cudaErrorInvalidValue;
     auto kern = fa_fwd_tc_kernel<D, CAUSAL, OUT_F32, SPARSE>;
