@@ -531,7 +531,7 @@ def run_ours(args, rank, world, local):
         e2e = {"value": job_flops * Ke / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
                "steps": Ke, "ms_per_step": e2e_ms / Ke,
-               "api": "fa_fwd_host (pinned host buffers, copies overlapped over 4 groups of (b, h) slices)"}
+               "api": "fa_fwd_host (pinned host buffers, copies overlapped over 8 groups of (b, h) slices)"}
 
     if rank != 0:
         return None

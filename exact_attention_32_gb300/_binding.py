@@ -23,7 +23,7 @@ _lock = threading.Lock()
 FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_NO_DEVICE",
                 4: "FA_ERR_ARCH", 5: "FA_ERR_LAUNCH", 6: "FA_ERR_TIMEOUT", 7: "FA_ERR_WORKSPACE_LIMIT"}
-EXPORTED = ("fa_fwd", "fa_fwd_kernel", "fa_bh_partition", "fa_fwd_slab", "fa_fwd_host", "fa_fwd_mma", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_combine",
+EXPORTED = ("fa_fwd", "fa_fwd_kernel", "fa_bh_partition", "fa_kv_shard", "fa_fwd_kv_shard", "fa_fwd_slab", "fa_fwd_host", "fa_fwd_mma", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_combine",
             "fa_fwd_splitkv_noalloc", "fa_fwd_fp8", "fa_fwd_blocksparse", "fa_bwd", "fa_bwd_workspace_bytes", "fa_get_device_status",
             "fa_status_string", "fa_version")
 
@@ -51,6 +51,11 @@ def lib():
             L.fa_fwd_kernel.argtypes = [i64, i64, i64, i64, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
             L.fa_bh_partition.restype = ctypes.c_int
             L.fa_bh_partition.argtypes = [i64, i64, i64, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+            L.fa_kv_shard.restype = ctypes.c_int
+            L.fa_kv_shard.argtypes = [i64, i64, i64, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+            L.fa_fwd_kv_shard.restype = ctypes.c_int
+            L.fa_fwd_kv_shard.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float, ctypes.c_int,
+                                          i64, i64, vp]
             L.fa_fwd_slab.restype = ctypes.c_int
             L.fa_fwd_slab.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float, ctypes.c_int,
                                       i64, i64, vp]
@@ -114,6 +119,22 @@ def fa_bh_partition(n_slices: int, world: int, rank: int):
     if st != FA_OK:
         raise FAError(st, "fa_bh_partition")
     return begin.value, count.value
+
+
+def fa_kv_shard(N: int, world: int, rank: int):
+    """(begin, count): the keys of every (b, h) slice that rank ``rank`` of
+    ``world`` holds in a sequence-sharded problem (pure host computation in the
+    library).  Raises FAError on invalid arguments."""
+    begin, count = ctypes.c_int64(0), ctypes.c_int64(0)
+    st = lib().fa_kv_shard(int(N), int(world), int(rank), ctypes.byref(begin), ctypes.byref(count))
+    if st != FA_OK:
+        raise FAError(st, "fa_kv_shard")
+    return begin.value, count.value
+
+
+def fa_fwd_kv_shard(q, k_shard, v_shard, o_part, lse_part, B, H, N, d, scale, causal, rank, world, stream) -> int:
+    return lib().fa_fwd_kv_shard(q, k_shard, v_shard, o_part, lse_part, B, H, N, d, scale, int(causal), rank,
+                                 world, stream)
 
 
 def fa_fwd_slab(q, k, v, o, lse, B, H, N, d, scale, causal, rank, world, stream) -> int:
@@ -329,6 +350,61 @@ def combine(o_parts: torch.Tensor, lse_parts: torch.Tensor, stream: torch.cuda.S
     if st != FA_OK:
         raise FAError(st, "fa_combine")
     return o, lse
+
+
+def forward_kv_shard(q: torch.Tensor, k_shard: torch.Tensor | None, v_shard: torch.Tensor | None, rank: int,
+                     world: int, scale: float | None = None, causal: bool = False,
+                     stream: torch.cuda.Stream | None = None):
+    """This rank's partial (O fp32 [B, H, N, d], LSE fp32 [B, H, N]) of a
+    sequence-sharded forward by ``fa_fwd_kv_shard``: all query rows of q
+    against the keys ``fa_kv_shard(N, world, rank)`` gives, held in k_shard and
+    v_shard ([B, H, count, d] bf16 CUDA tensors; None when count is 0)."""
+    if q.dim() != 4 or q.dtype != torch.bfloat16 or not q.is_cuda or not q.is_contiguous():
+        raise ValueError("q must be a contiguous bf16 CUDA tensor [B, H, N, d]")
+    B, H, N, d = q.shape
+    begin, count = fa_kv_shard(N, world, rank)
+    if count > 0:
+        for t in (k_shard, v_shard):
+            if (t is None or t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous()
+                    or tuple(t.shape) != (B, H, count, d)):
+                raise ValueError(f"k_shard and v_shard must be contiguous bf16 CUDA tensors [{B}, {H}, {count}, {d}]")
+    scale = default_scale(d) if scale is None else scale
+    o_part = torch.empty((B, H, N, d), dtype=torch.float32, device=q.device)
+    lse_part = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    kp = k_shard.data_ptr() if count > 0 else None
+    vp = v_shard.data_ptr() if count > 0 else None
+    with torch.cuda.device(q.device):
+        st = fa_fwd_kv_shard(q.data_ptr(), kp, vp, o_part.data_ptr(), lse_part.data_ptr(), B, H, N, d, scale,
+                             causal, rank, world, s.cuda_stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_kv_shard")
+    return o_part, lse_part
+
+
+def gather_parts(o_part: torch.Tensor, lse_part: torch.Tensor, group=None):
+    """The exchange step of a sequence-sharded forward: all-gather every rank's
+    partial (O, LSE) over ``torch.distributed`` into ([world, ...], [world, ...])
+    tensors, in rank order, ready for ``combine``."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    o_list = [torch.empty_like(o_part) for _ in range(world)]
+    lse_list = [torch.empty_like(lse_part) for _ in range(world)]
+    dist.all_gather(o_list, o_part.contiguous(), group=group)
+    dist.all_gather(lse_list, lse_part.contiguous(), group=group)
+    return torch.stack(o_list), torch.stack(lse_list)
+
+
+def forward_sequence_sharded(q: torch.Tensor, k_shard: torch.Tensor | None, v_shard: torch.Tensor | None,
+                             scale: float | None = None, causal: bool = False, group=None):
+    """(O bf16, LSE) of the whole problem on every rank of ``group``: this
+    rank's partial (``forward_kv_shard``), the all-gather of the parts
+    (``gather_parts``), and their merge (``combine``)."""
+    import torch.distributed as dist
+    rank, world = dist.get_rank(group), dist.get_world_size(group)
+    o_part, lse_part = forward_kv_shard(q, k_shard, v_shard, rank, world, scale=scale, causal=causal)
+    o_parts, lse_parts = gather_parts(o_part, lse_part, group)
+    return combine(o_parts, lse_parts)
 
 
 def backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,

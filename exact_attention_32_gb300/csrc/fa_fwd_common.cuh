@@ -47,11 +47,14 @@ __device__ __forceinline__ int unit_index(int r)
     return r * G + ((r & 1) ? (G - 1 - c) : c);
 }
 
-// SPLIT: the launch covers key splits (the split-KV partials); otherwise every
-// item spans all N keys, and the split fields are compile-time constants, so
-// the single-split variants carry none of the key-range arithmetic.
+// SPLIT: the launch covers key splits split0 .. split0 + n_splits - 1 (the
+// split-KV partials; split0 > 0 when one GPU computes one split of a sequence
+// sharded over several); otherwise every item spans all N keys, and the split
+// fields are compile-time constants, so the single-split variants carry none of
+// the key-range arithmetic.  `split` is the index within the launch.
 template <bool CAUSAL, bool SPLIT, bool GROUPED>
-__device__ __forceinline__ Unit unit_of(int u, int N, int BH, int n_mblocks, int n_splits, int kv_chunk, int hg)
+__device__ __forceinline__ Unit unit_of(int u, int N, int BH, int n_mblocks, int n_splits, int kv_chunk, int hg,
+                                        int split0 = 0)
 {
     Unit w;
     if constexpr (!SPLIT) {
@@ -80,7 +83,7 @@ __device__ __forceinline__ Unit unit_of(int u, int N, int BH, int n_mblocks, int
     const int mb = CAUSAL ? (n_mblocks - 1 - rb / BH) : (rb / BH);
     w.bh = rb % BH;
     w.q_row0 = mb * (kQTiles * kBlockM);
-    w.kv_begin = w.split * kv_chunk;
+    w.kv_begin = (split0 + w.split) * kv_chunk;
     w.kv_end = min(N, w.kv_begin + kv_chunk);
     // keys any row of this block admits end before k_hi
     const int k_hi = CAUSAL ? min(w.kv_end, w.q_row0 + kQTiles * kBlockM) : w.kv_end;

@@ -190,7 +190,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                  void *__restrict__ o, float *__restrict__ lse, int N, int BH, int n_mblocks, int n_units,
                  int n_splits, int kv_chunk, int hg, float scale, float scale_log2, const uint8_t *__restrict__ bm,
-                 int nb)
+                 int nb, int split0)
 {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -260,7 +260,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             bool ok = true;
             int it = 0, uc = 0;
             for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
-                const Unit w = unit_of<CAUSAL, OUT_F32, !SPARSE>(u, N, BH, n_mblocks, n_splits, kv_chunk, hg);
+                const Unit w = unit_of<CAUSAL, OUT_F32, !SPARSE>(u, N, BH, n_mblocks, n_splits, kv_chunk, hg, split0);
                 if (!SPARSE && w.n_kv <= 0) continue;  // a key split with no admitted key: nothing to load
                 // block-sparse: the live tiles in order, each published in its K slot's record
                 // with its admission bits and a last-tile flag (found by looking one live
@@ -323,9 +323,11 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         if (SPARSE && kind == 0) kv_meta[slot] = meta;  // released by the arrive below
                         mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
                         const CUtensorMap *tm = kind == 0 ? &tm_k : &tm_v;
+                        // K and V rows from the first key of split split0 on (a sequence shard's own rows)
                         for (int a = 0; a < C::kAtoms; ++a)
                             tma_load_3d(sRing + slot * C::kTileBytes + a * 16384, tm, bars.full(slot),
-                                        a * (128 / C::kElem), (w.j0 + j) * kBlockN, w.bh);
+                                        a * (128 / C::kElem), (w.j0 + j) * kBlockN - (OUT_F32 ? split0 * kv_chunk : 0),
+                                        w.bh);
                     }
                 }
             }
@@ -363,7 +365,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 return mbar_wait(bars.p_full(t), ((t ? jg1 : jg0) - 1) & 1, kWaitLimitNs);
             };
             for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
-                const Unit w = unit_of<CAUSAL, OUT_F32, !SPARSE>(u, N, BH, n_mblocks, n_splits, kv_chunk, hg);
+                const Unit w = unit_of<CAUSAL, OUT_F32, !SPARSE>(u, N, BH, n_mblocks, n_splits, kv_chunk, hg, split0);
                 if (!SPARSE && w.n_kv <= 0) continue;  // a key split with no admitted key
                 if constexpr (SPARSE) {
                     // a unit with no live tile: its one record goes to both softmax warpgroups
@@ -486,7 +488,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         bool ok = true;
         int jg = 0, uc = 0;
         for (int r = 0, u = unit_index(0); u < n_units && ok; u = unit_index(++r)) {
-            const Unit w = unit_of<CAUSAL, OUT_F32, !SPARSE>(u, N, BH, n_mblocks, n_splits, kv_chunk, hg);
+            const Unit w = unit_of<CAUSAL, OUT_F32, !SPARSE>(u, N, BH, n_mblocks, n_splits, kv_chunk, hg, split0);
             const int row_g = w.q_row0 + t * kBlockM + row;
             auto out_row_of = [&]() { return (static_cast<int64_t>(w.split) * BH + w.bh) * N + row_g; };
             const bool qb_ok = !SPARSE || (w.q_row0 / kBlockM + t < nb);
@@ -762,16 +764,24 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
 // ------------------------------------------------------------------ host side
 
+// kv_rows: rows of K and V per slice (N unless they hold one sequence shard:
+// the keys of splits split0 .. split0 + n_splits - 1 only; 0 for a shard past
+// the last key, whose K and V are never read).
 template <int D, bool CAUSAL, bool OUT_F32, bool SPARSE = false>
 cudaError_t launch(const FaProblem &p, void *o, float *lse, int n_splits, int kv_chunk, cudaStream_t stream,
-                   const uint8_t *bm = nullptr)
+                   const uint8_t *bm = nullptr, int split0 = 0, int64_t kv_rows = -1)
 {
     using C = Cfg<D>;
     CUtensorMap mq, mk, mv, mo;
     const int64_t BH = p.B * p.H;
-    if (!make_map(&mq, p.q, BH, p.N, D, C::kElem) || !make_map(&mk, p.k, BH, p.N, D, C::kElem) ||
-        !make_map(&mv, p.v, BH, p.N, D, C::kElem))
+    if (kv_rows < 0) kv_rows = p.N;
+    if (!make_map(&mq, p.q, BH, p.N, D, C::kElem)) return cudaErrorInvalidValue;
+    if (kv_rows == 0) {
+        mk = mq;
+        mv = mq;
+    } else if (!make_map(&mk, p.k, BH, kv_rows, D, C::kElem) || !make_map(&mv, p.v, BH, kv_rows, D, C::kElem)) {
         return cudaErrorInvalidValue;
+    }
     if (OUT_F32)
         mo = mq;  // not used: the key-split partials store O directly
     else if (!make_out_map(&mo, o, BH, p.N, D))
@@ -797,18 +807,19 @@ cudaError_t launch(const FaProblem &p, void *o, float *lse, int n_splits, int kv
     kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
         mq, mk, mv, mo, o, lse, static_cast<int>(p.N), static_cast<int>(BH), static_cast<int>(n_mblocks),
         static_cast<int>(n_units), n_splits, kv_chunk, static_cast<int>(hg), p.scale, scale_log2, bm,
-        static_cast<int>((p.N + kBlockN - 1) / kBlockN));
+        static_cast<int>((p.N + kBlockN - 1) / kBlockN), split0);
     return cudaGetLastError();
 }
 
 template <bool OUT_F32>
-cudaError_t dispatch(const FaProblem &p, void *o, float *lse, int n_splits, int kv_chunk, cudaStream_t s)
+cudaError_t dispatch(const FaProblem &p, void *o, float *lse, int n_splits, int kv_chunk, cudaStream_t s,
+                     int split0 = 0, int64_t kv_rows = -1)
 {
     if (p.d == 64)
-        return p.causal ? launch<64, true, OUT_F32>(p, o, lse, n_splits, kv_chunk, s)
-                        : launch<64, false, OUT_F32>(p, o, lse, n_splits, kv_chunk, s);
-    return p.causal ? launch<128, true, OUT_F32>(p, o, lse, n_splits, kv_chunk, s)
-                    : launch<128, false, OUT_F32>(p, o, lse, n_splits, kv_chunk, s);
+        return p.causal ? launch<64, true, OUT_F32>(p, o, lse, n_splits, kv_chunk, s, nullptr, split0, kv_rows)
+                        : launch<64, false, OUT_F32>(p, o, lse, n_splits, kv_chunk, s, nullptr, split0, kv_rows);
+    return p.causal ? launch<128, true, OUT_F32>(p, o, lse, n_splits, kv_chunk, s, nullptr, split0, kv_rows)
+                    : launch<128, false, OUT_F32>(p, o, lse, n_splits, kv_chunk, s, nullptr, split0, kv_rows);
 }
 
 }  // namespace
@@ -837,9 +848,9 @@ cudaError_t fa_launch_tc(const FaProblem &p, cudaStream_t stream)
 }
 
 cudaError_t fa_launch_tc_partials(const FaProblem &p, float *o_parts, float *lse_parts, int n_splits, int kv_chunk,
-                                  cudaStream_t stream)
+                                  cudaStream_t stream, int split0, int64_t kv_rows)
 {
-    return dispatch<true>(p, o_parts, lse_parts, n_splits, kv_chunk, stream);
+    return dispatch<true>(p, o_parts, lse_parts, n_splits, kv_chunk, stream, split0, kv_rows);
 }
 
 cudaError_t fa_launch_tc_sparse(const FaProblem &p, const uint8_t *block_mask, cudaStream_t stream)

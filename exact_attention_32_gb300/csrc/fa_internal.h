@@ -48,9 +48,11 @@ struct FaProblem {
 cudaError_t fa_launch_tc(const FaProblem &p, cudaStream_t stream);
 bool fa_fwd_takes_dp(int64_t N, int64_t d, int causal);
 // The same kernel over n_splits key ranges of kv_chunk keys (a multiple of
-// 128): split s writes fp32 O to o_parts + s*B*H*N*d and LSE to lse_parts + s*B*H*N.
+// 128): split s (keys from (split0 + s) * kv_chunk) writes fp32 O to
+// o_parts + s*B*H*N*d and LSE to lse_parts + s*B*H*N.  K and V hold kv_rows rows
+// per slice starting at key split0 * kv_chunk (default: all N keys, split0 = 0).
 cudaError_t fa_launch_tc_partials(const FaProblem &p, float *o_parts, float *lse_parts, int n_splits, int kv_chunk,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, int split0 = 0, int64_t kv_rows = -1);
 // The same kernel restricted by a [ceil(N/128)]^2 0/1 block mask over (query block, key block).
 cudaError_t fa_launch_tc_sparse(const FaProblem &p, const uint8_t *block_mask, cudaStream_t stream);
 // The kernel with P apart from S (fa_fwd_dp.cu): bf16 at d = 64 (taken by

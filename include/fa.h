@@ -150,7 +150,7 @@ int fa_fwd_slab(const void *q, const void *k, const void *v, void *o, float *lse
  *             return from a completed call they hold the inputs and outputs.
  *   n_groups: the B*H (b, h) slices are processed in n_groups consecutive
  *             groups of near-equal size (1 <= n_groups <= min(B*H, 64); 0
- *             selects min(B*H, 4)).  Group g+1's copies in overlap group g's
+ *             selects min(B*H, 8)).  Group g+1's copies in overlap group g's
  *             forward, and group g's copies out overlap group g+1's forward.
  *   stream  : the copies in start after the work already queued on `stream`;
  *             work queued on `stream` afterwards starts after the last copy
@@ -240,6 +240,51 @@ int64_t fa_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t 
 int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
                            int64_t B, int64_t H, int64_t N, int64_t d, float scale,
                            int causal, int64_t n_splits, void *stream);
+
+/*
+ * fa_kv_shard - the keys one GPU of a sequence-sharded problem holds: rank r
+ * of `world` takes keys [begin, begin + count) of every (b, h) slice, the key
+ * range of split r in fa_fwd_splitkv with n_splits = world (ranges of
+ * 128 * ceil(ceil(N / world) / 128) keys; ranks past the last key get
+ * count = 0).
+ *
+ *   N : keys (= queries) per slice, >= 1;  world : 1..32;  0 <= rank < world
+ *   begin, count : host outputs
+ * Pure host computation.  Returns FA_OK, or FA_ERR_INVALID_ARG (nothing
+ * written) for out-of-range arguments or a null output pointer.
+ */
+int fa_kv_shard(int64_t N, int64_t world, int64_t rank, int64_t *begin, int64_t *count);
+
+/*
+ * fa_fwd_kv_shard - one GPU's part of a sequence-sharded forward: every query
+ * row against the keys of this rank's shard only, as a partial result that
+ * fa_combine merges with the other ranks' parts.  The pages split a row's keys
+ * into blocks whose (max, sum, output) merge exactly ("FlashAttention:
+ * IO-Aware Tiling, Online Softmax Mathematics, ...", section "Online Softmax
+ * Mathematics", the two-block merge); spread over GPUs, that merge is
+ * the one exchange a sequence-sharded attention needs.  Gathering the parts
+ * (an all-gather of o_part and lse_part) is the caller's; the merge is
+ * fa_combine on the gathered [world] parts.
+ *
+ *   q        : const bf16 [B][H][N][d], all query rows.
+ *   k_shard, v_shard : const bf16 [B][H][count][d], keys begin .. begin +
+ *              count - 1 of each slice (fa_kv_shard); may be NULL when count = 0.
+ *   o_part   : fp32 out [B][H][N][d], O over the shard's keys (normalised by
+ *              their sum).
+ *   lse_part : fp32 out [B][H][N], LSE over the shard's keys; a row with no
+ *              admitted key in the shard (causal rows before it, or an empty
+ *              shard) gets O = 0, LSE = -inf.
+ *   B, H, N, d, scale, causal : as for fa_fwd (causal compares absolute
+ *              positions: key begin + j against query i).
+ *   rank, world : as for fa_kv_shard.
+ * Pointers as for fa_fwd (lse_part 4-byte aligned, the rest 16-byte); the
+ * outputs must not overlap the inputs or each other.  Errors as fa_fwd, plus
+ * FA_ERR_INVALID_ARG for a bad rank or world.  On one GPU, the parts of all
+ * ranks merged by fa_combine equal fa_fwd_splitkv with n_splits = world.
+ */
+int fa_fwd_kv_shard(const void *q, const void *k_shard, const void *v_shard, float *o_part,
+                    float *lse_part, int64_t B, int64_t H, int64_t N, int64_t d, float scale,
+                    int causal, int64_t rank, int64_t world, void *stream);
 
 /*
  * fa_combine - merge n_parts partial attention results of the same rows over

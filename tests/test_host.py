@@ -46,7 +46,7 @@ def test_host_forward_matches_oracle(B, H, N, d, causal, groups, pinned):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("name,groups", [("b2_h32_n4096_d128_causal", 4), ("b4_h16_n2048_d128", 7),
-                                         ("b16_h16_n1000_d64_causal_q8", 64)])
+                                         ("b16_h16_n1000_d64_causal_q8", 64), ("b1_h32_n16384_d128_causal", 0)])
 def test_host_forward_bit_identical_to_device_forward(name, groups):
     w = WORKLOADS[name]
     q, k, v = (t.pin_memory() for t in workload_inputs(w))
