@@ -272,39 +272,35 @@ fa_fwd_dp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     break;
                 }
                 tc_fence_after();
-                float s[kBlockN];
-                {
-                    uint32_t rr[4][32];
+                // S_t, each 32-column piece's max coming with the load
+                float s[kBlockN], pm[4];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, rr[c]);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(rr[c][i]);
-                }
+                for (int c = 0; c < 4; ++c)
+                    tmem_ld32_max(tS + c * 32, *reinterpret_cast<float(*)[32]>(&s[c * 32]), pm[c]);
+                tmem_wait_ld();
                 // S_t is in registers: the next S may overwrite it
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bars.s_free(t));
+                float mt = fmax3(fmaxf(pm[0], pm[1]), pm[2], pm[3]);
                 const int k0 = j * kBlockN;
                 if (k0 + kBlockN > N || (CAUSAL && k0 + kBlockN - 1 > w.q_row0 + t * kBlockM)) {
+                    // masked keys: the max again over the admitted ones
                     const int lim = CAUSAL ? min(N - 1, row_g) : N - 1;
 #pragma unroll
                     for (int i = 0; i < kBlockN; ++i)
                         if (k0 + i > lim) s[i] = -INFINITY;
-                }
-                float mx[8];
+                    float mx[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int b0 = 16 * q;
-                    float a = fmax3(s[b0], s[b0 + 1], s[b0 + 2]);
+                    for (int q = 0; q < 8; ++q) {
+                        const int b0 = 16 * q;
+                        float a = fmax3(s[b0], s[b0 + 1], s[b0 + 2]);
 #pragma unroll
-                    for (int i = 3; i < 15; i += 2) a = fmax3(a, s[b0 + i], s[b0 + i + 1]);
-                    mx[q] = fmaxf(a, s[b0 + 15]);
+                        for (int i = 3; i < 15; i += 2) a = fmax3(a, s[b0 + i], s[b0 + i + 1]);
+                        mx[q] = fmaxf(a, s[b0 + 15]);
+                    }
+                    mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
                 }
-                const float mt =
-                    fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
                 const float m_new = fmaxf(m_ref, mt);
                 const bool need = (m_new - m_ref) * c_u > kRescaleLog2;  // true while m_ref = -inf
                 float alpha = 1.f;

@@ -184,6 +184,29 @@ __device__ __forceinline__ bool tile0_skips_last(const Unit &w, int N)
 // SPARSE: bm is a [nb][nb] 0/1 block mask (nb = ceil(N/128)) over (query block,
 // key block); K/V tiles no query block of the unit admits are skipped, and a
 // tile is fully masked for a query tile whose block does not admit it.
+// Keys outside [lo, hi] of the tile starting at key k0 to -inf.
+__device__ __forceinline__ void mask_keys(float (&s)[kBlockN], int k0, int lo, int hi)
+{
+#pragma unroll
+    for (int i = 0; i < kBlockN; ++i)
+        if (k0 + i < lo || k0 + i > hi) s[i] = -INFINITY;
+}
+
+// Row max of a tile: eight independent chains of 3-input maxes.
+__device__ __forceinline__ float row_max(const float (&s)[kBlockN])
+{
+    float mx[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        const int b = 16 * g;
+        float a = fmax3(s[b], s[b + 1], s[b + 2]);
+#pragma unroll
+        for (int i = 3; i < 15; i += 2) a = fmax3(a, s[b + i], s[b + i + 1]);
+        mx[g] = fmaxf(a, s[b + 15]);
+    }
+    return fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+}
+
 template <int D, bool CAUSAL, bool OUT_F32, bool SPARSE>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -540,8 +563,12 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tc_fence_after();
                 const uint32_t meta = SPARSE ? s_meta[t] : 0u;
                 const int j = SPARSE ? static_cast<int>(meta & kMetaTile) : jc;
-                float s[kBlockN];
-                {
+                // S_t and its row max over the admitted keys
+                float s[kBlockN], mt;
+                const int k0 = (w.j0 + j) * kBlockN;
+                const bool need_mask = k0 < w.kv_begin || k0 + kBlockN > w.kv_end ||
+                                       (CAUSAL && k0 + kBlockN - 1 > w.q_row0 + t * kBlockM);
+                if constexpr (SPARSE) {  // (registers at their limit: the plain load and max pass)
                     uint32_t r[4][32];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, r[c]);
@@ -550,33 +577,26 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     for (int c = 0; c < 4; ++c)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
-                }
-                const int k0 = (w.j0 + j) * kBlockN;
-                if (SPARSE && (!qb_ok || (meta & kMetaOwn0) == 0u)) {
+                    if (!qb_ok || (meta & kMetaOwn0) == 0u) {
 #pragma unroll
-                    for (int i = 0; i < kBlockN; ++i) s[i] = -INFINITY;  // block not admitted for this query tile
-                }
-                const bool need_mask = k0 < w.kv_begin || k0 + kBlockN > w.kv_end ||
-                                       (CAUSAL && k0 + kBlockN - 1 > w.q_row0 + t * kBlockM);
-                if (need_mask) {
-                    // admitted keys: kv_begin <= key <= lim
-                    const int lim = CAUSAL ? min(w.kv_end - 1, row_g) : w.kv_end - 1;
+                        for (int i = 0; i < kBlockN; ++i) s[i] = -INFINITY;  // block not admitted for this query tile
+                    }
+                    if (need_mask) mask_keys(s, k0, w.kv_begin, CAUSAL ? min(w.kv_end - 1, row_g) : w.kv_end - 1);
+                    mt = row_max(s);
+                } else {
+                    // each 32-column piece's max comes with the load; a tile with masked keys
+                    // takes the max again over the admitted ones
+                    float pm[4];
 #pragma unroll
-                    for (int i = 0; i < kBlockN; ++i)
-                        if (k0 + i < w.kv_begin || k0 + i > lim) s[i] = -INFINITY;
+                    for (int c = 0; c < 4; ++c)
+                        tmem_ld32_max(tS + c * 32, *reinterpret_cast<float(*)[32]>(&s[c * 32]), pm[c]);
+                    tmem_wait_ld();
+                    mt = fmax3(fmaxf(pm[0], pm[1]), pm[2], pm[3]);
+                    if (need_mask) {
+                        mask_keys(s, k0, w.kv_begin, CAUSAL ? min(w.kv_end - 1, row_g) : w.kv_end - 1);
+                        mt = row_max(s);
+                    }
                 }
-                // row max: eight independent chains of 3-input maxes
-                float mx[8];
-#pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    const int b = 16 * g;
-                    float a = fmax3(s[b], s[b + 1], s[b + 2]);
-#pragma unroll
-                    for (int i = 3; i < 15; i += 2) a = fmax3(a, s[b + i], s[b + i + 1]);
-                    mx[g] = fmaxf(a, s[b + 15]);
-                }
-                const float mt =
-                    fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
                 const float m_new = fmaxf(m_ref, mt);
                 const bool need = (m_new - m_ref) * c_u > kRescaleLog2;  // true while m_ref = -inf
                 float alpha = 1.f;

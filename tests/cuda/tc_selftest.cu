@@ -174,3 +174,45 @@ extern "C" int wait_timeout_selftest(int *status, unsigned long long limit_ns, u
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     return static_cast<int>(e);
 }
+
+// tcgen05.ld with a max reduction: 128 threads store rows of 128 fp32 values
+// (in[128][128]) into tensor memory columns [0, 128), load them back in four
+// 32-column pieces with tmem_ld32_max, and write the values (out_vals) and
+// each piece's reported maximum (out_max[128][4]).
+__global__ void __launch_bounds__(128, 1) ld_max_kernel(const float *in, float *out_vals, float *out_max)
+{
+    __shared__ uint32_t slot;
+    const int tid = threadIdx.x, warp = tid / 32;
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&slot), 128);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t t = slot + (static_cast<uint32_t>(warp * 32) << 16);
+    for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(in[tid * 128 + c * 32 + i]);
+        tmem_st32(t + c * 32, r);
+    }
+    tmem_wait_st();
+    for (int c = 0; c < 4; ++c) {
+        float v[32], m;
+        tmem_ld32_max(t + c * 32, v, m);
+        tmem_wait_ld();
+        for (int i = 0; i < 32; ++i) out_vals[tid * 128 + c * 32 + i] = v[i];
+        out_max[tid * 4 + c] = m;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(slot, 128);
+}
+
+extern "C" int ld_max_selftest(const float *in, float *out_vals, float *out_max)
+{
+    ld_max_kernel<<<1, 128>>>(in, out_vals, out_max);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    return static_cast<int>(e);
+}

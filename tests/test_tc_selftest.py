@@ -69,3 +69,24 @@ def test_bounded_wait_gives_up_and_context_survives(selftest_lib):
     assert limit_ns <= int(elapsed.item()) < 20 * limit_ns
     x = torch.arange(1000, device="cuda", dtype=torch.float32)
     assert float(x.sum().item()) == 499500.0
+
+
+def test_tensor_memory_load_with_max(selftest_lib):
+    # the reducing tensor-memory load returns the values unchanged and, per
+    # thread, the largest of the 32 it loaded; rows hold negative values,
+    # -inf (masked keys), all--inf pieces and ties
+    selftest_lib.ld_max_selftest.restype = ctypes.c_int
+    selftest_lib.ld_max_selftest.argtypes = [ctypes.c_void_p] * 3
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn((128, 128), generator=g) * 30
+    x[::3, 5::7] = float("-inf")
+    x[5, 32:64] = float("-inf")
+    x[9, :] = -1.0
+    x[11, 70] = 1e30
+    x[12, 96:128] = -3.5
+    xd = x.cuda()
+    vals = torch.empty_like(xd)
+    mx = torch.empty((128, 4), device="cuda")
+    assert selftest_lib.ld_max_selftest(xd.data_ptr(), vals.data_ptr(), mx.data_ptr()) == 0
+    assert torch.equal(vals.cpu(), x)
+    assert torch.equal(mx.cpu(), x.view(128, 4, 32).amax(dim=2))
