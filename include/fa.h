@@ -279,8 +279,10 @@ int fa_kv_shard(int64_t N, int64_t world, int64_t rank, int64_t *begin, int64_t 
  *   rank, world : as for fa_kv_shard.
  * Pointers as for fa_fwd (lse_part 4-byte aligned, the rest 16-byte); the
  * outputs must not overlap the inputs or each other.  Errors as fa_fwd, plus
- * FA_ERR_INVALID_ARG for a bad rank or world.  On one GPU, the parts of all
- * ranks merged by fa_combine equal fa_fwd_splitkv with n_splits = world.
+ * FA_ERR_INVALID_ARG for a bad rank or world, or a rank whose key range would
+ * pass 2^31.  Gathered on one GPU, the parts of all ranks merged by fa_combine
+ * give fa_fwd_splitkv's result with n_splits = world (bit for bit when every
+ * rank holds keys; ranks without keys add parts of weight 0).
  */
 int fa_fwd_kv_shard(const void *q, const void *k_shard, const void *v_shard, float *o_part,
                     float *lse_part, int64_t B, int64_t H, int64_t N, int64_t d, float scale,
