@@ -64,6 +64,10 @@ def parse_args():
     p.add_argument("--scaling", default="weak", choices=["weak", "strong"],
                    help="under torchrun: weak = N draws of the workload, one slab of B*H slices per rank; "
                         "strong = the workload's B*H slices split over the ranks")
+    p.add_argument("--shard", default="heads", choices=["heads", "seq"],
+                   help="under torchrun: heads = slabs of (b, h) slices, no exchange (the default); seq = every "
+                        "rank holds all queries and one key shard (fa_fwd_kv_shard), then an all-gather of the "
+                        "partial (O, LSE) and their merge (fa_combine); strong scaling over the workload's keys")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-secondary", action="store_true",
@@ -611,11 +615,101 @@ def run_reference(args, rank, world):
     }
 
 
+def run_seq_sharded(args, rank, world, local):
+    """The workload's keys split over the ranks: a step is this rank's partial
+    forward over its key shard, the all-gather of every rank's partial (O, LSE)
+    and their merge; timed with CUDA events around whole steps, max over ranks."""
+    import exact_attention_32_gb300 as fa
+    w = WORKLOADS[args.workload]
+    dev = torch.device("cuda", local if world > 1 else 0)
+    fa.lib()
+    q_h, k_h, v_h = workload_inputs(w)
+    begin, count = fa.fa_kv_shard(w.N, world, rank)
+    q = q_h.to(dev)
+    ks = k_h[:, :, begin:begin + count].contiguous().to(dev) if count else None
+    vs = v_h[:, :, begin:begin + count].contiguous().to(dev) if count else None
+    group = None
+    if world > 1:
+        import torch.distributed as dist
+        group = dist.group.WORLD
+    stream = torch.cuda.current_stream(dev)
+    part_ms = []
+
+    def step(record=False):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        o_part, lse_part = fa.forward_kv_shard(q, ks, vs, rank, world, scale=w.scale, causal=w.causal,
+                                               stream=stream)
+        e1.record(stream)
+        if world > 1:
+            o_parts, lse_parts = fa.gather_parts(o_part, lse_part, group)
+        else:
+            o_parts, lse_parts = o_part.unsqueeze(0), lse_part.unsqueeze(0)
+        out = fa.combine(o_parts, lse_parts, stream=stream)
+        if record:
+            part_ms.append((e0, e1))
+        return out
+
+    for _ in range(args.warmup):
+        step()
+    K = args.steps
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(K):
+        step(record=True)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    st = fa.fa_get_device_status(stream.cuda_stream)
+    if st != 0:
+        raise fa.FAError(st, "sequence-sharded step")
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    if rank != 0:
+        return None
+    part = statistics.mean(a.elapsed_time(b) for a, b in part_ms)  # rank 0's partial forward
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    # rank 0's partial forward: its keys against every query (causal: the
+    # admitted pairs only; rank 0's shard has the most)
+    lo, n = fa.fa_kv_shard(w.N, world, 0)
+    pairs = sum(min(n, max(0, i + 1 - lo)) for i in range(w.N)) if w.causal else w.N * n
+    part_flops = 4.0 * w.B * w.H * pairs * w.d
+    value = w.flops * K / (total_ms / 1e3) / 1e12
+    return {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: Q, K, V iid N(0,1) fp32 rounded to bf16, seeded",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "scale": w.scale, "global_batch": w.B, "seq_len": w.N, "parallelism": f"kv_shards{world}",
+                   "shard_rank0": {"begin": lo, "count": n},
+                   "step": "fa_fwd_kv_shard + all-gather of (O, LSE) parts + fa_combine"},
+        "roofline": {"bound": "tensor", "kernel": "fa_fwd_tc_kernel (key-shard partial)",
+                     "achieved": part_flops / (part / 1e3) / 1e12, "peak": peak,
+                     "peak_source": f"{peak_src} bf16_tflops (burst)", "unit": "TFLOP/s",
+                     "frac": part_flops / (part / 1e3) / 1e12 / peak, "traffic": None,
+                     "algorithmic_flops_per_launch": part_flops, "launch_ms": part},
+        "gpu_launches": 2 * K,
+        "clocks": clk,
+        "impl": "ours",
+    }
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_setup(args)
     if args.impl == "reference":
         line = run_reference(args, rank, world)
+    elif args.shard == "seq":
+        line = run_seq_sharded(args, rank, world, local)
     else:
         line = run_ours(args, rank, world, local)
     if line is not None:
