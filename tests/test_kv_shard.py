@@ -157,3 +157,32 @@ def test_shards_merge_to_the_whole_result(N, world, d, causal):
         assert torch.equal(o, o_s) and torch.equal(lse, lse_s)
     else:
         assert (o.float() - o_s.float()).abs().max().item() <= 2 ** -7
+
+
+def _nccl_one_rank_worker(rank, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+    import exact_attention_32_gb300 as fa
+    from exact_attention_32_gb300 import make_inputs
+    torch.cuda.set_device(0)
+    dist.init_process_group("nccl", rank=0, world_size=1)
+    q, k, v = make_inputs(2, 3, 700, 128, seed=77)
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    o, lse = fa.forward_sequence_sharded(qc, kc, vc, scale=0.08838834764831845, causal=True)
+    o_s, lse_s, _ = fa.forward_splitkv(qc, kc, vc, 1, scale=0.08838834764831845, causal=True)
+    torch.cuda.synchronize()
+    out["equal"] = bool(torch.equal(o, o_s) and torch.equal(lse, lse_s))
+    out["status"] = fa.fa_get_device_status(0)
+    dist.destroy_process_group()
+
+
+@pytest.mark.gpu
+def test_sequence_sharded_forward_through_nccl_on_one_rank():
+    # the product function end to end: the shard forward, the NCCL all-gather
+    # (one rank) and the merge give the split-KV forward's result bit for bit
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    mp.start_processes(_nccl_one_rank_worker, args=(free_port(), out), nprocs=1, join=True, start_method="spawn")
+    assert out["status"] == 0 and out["equal"]
