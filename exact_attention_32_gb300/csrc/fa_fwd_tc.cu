@@ -36,15 +36,17 @@
 // "6.1 ...", section 3.3 - so a stale reference is exact as long as the
 // exponentials stay in range; LSE = m_ref + ln(l) holds for any reference).
 // Keys >= N and, when causal, keys j > i are set to -inf before the max
-// ("6.1 ...", section 8.3: the K/V out-of-range mask).
+// ("6.1 ...", section 8.3: the K/V out-of-range mask).  The row max of a tile
+// with no masked key comes with the tensor-memory load of S (tcgen05.ld with
+// a max reduction, sm_103a); a masked tile takes it again after masking.
 //
 // The epilogue (O / l to bf16) goes through shared memory: each softmax warp
 // writes 32-column chunks of its 32 rows there and one thread stores each
 // chunk with a TMA store, so global memory sees whole 64-byte row pieces
 // rather than one 16-byte piece of 32 different rows per instruction; the
 // tensor map clips the rows past N.  LSE is stored directly (a warp's 32 rows
-// are contiguous).  The fp32 partials of a key split and the block-sparse
-// forward store directly from registers.
+// are contiguous).  The fp32 partials of a key split store directly from
+// registers.
 //
 // fa_fwd_tc_kernel serves bf16 at d = 64 and 128 with its key-split and
 // block-sparse variants; fa_fwd_dp.cu holds the kernel that keeps P apart from
