@@ -133,6 +133,7 @@ def fa_kv_shard(N: int, world: int, rank: int):
 
 
 def fa_fwd_kv_shard(q, k_shard, v_shard, o_part, lse_part, B, H, N, d, scale, causal, rank, world, stream) -> int:
+    """Raw call of one rank's partial forward over its key shard."""
     return lib().fa_fwd_kv_shard(q, k_shard, v_shard, o_part, lse_part, B, H, N, d, scale, int(causal), rank,
                                  world, stream)
 
@@ -433,6 +434,31 @@ def backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     if st != FA_OK:
         raise FAError(st, "fa_bwd")
     return dq, dk, dv
+
+
+class _Attention(torch.autograd.Function):
+    """fa_fwd in the forward, fa_bwd in the backward (O and LSE saved)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, scale, causal):
+        o, lse = forward(q, k, v, scale=scale, causal=causal)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.scale, ctx.causal = scale, causal
+        return o
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = backward(q, k, v, o, lse, dout.contiguous(), scale=ctx.scale, causal=ctx.causal)
+        return dq, dk, dv, None, None
+
+
+def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
+              causal: bool = False) -> torch.Tensor:
+    """O = attention(q, k, v) with autograd: ``fa_fwd`` forward, ``fa_bwd``
+    backward (dQ, dK, dV of the loss through O).  q, k, v: contiguous bf16
+    CUDA tensors [B, H, N, d] (d = 64 or 128)."""
+    return _Attention.apply(q, k, v, default_scale(q.shape[-1]) if scale is None else scale, bool(causal))
 
 
 def forward_fp8(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale: torch.Tensor,

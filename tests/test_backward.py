@@ -102,3 +102,25 @@ def test_deterministic_dk_dv():
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
     # dQ sums partials from several CTAs with atomics: equal up to rounding order
     assert (a[0].float() - b[0].float()).abs().max().item() <= 2 ** -6 * a[0].float().abs().max().item()
+
+
+@pytest.mark.parametrize("d,causal", [(64, True), (128, False)])
+def test_autograd_attention(d, causal):
+    # attention() through torch.autograd: the loss sum(O * dO) backpropagates
+    # through fa_bwd to the oracle's gradients, and to the direct calls' dK and dV
+    # bit for bit (dQ is summed by reductions in L2, in no fixed order)
+    import exact_attention_32_gb300 as fa
+    q, k, v = make_inputs(1, 3, 300, d, seed=4100 + d)
+    do = make_grad_output(1, 3, 300, d, seed=4100 + d)
+    scale = float(np.float32(1 / np.sqrt(d)))
+    qd, kd, vd = (t.cuda().requires_grad_(True) for t in (q, k, v))
+    o = fa.attention(qd, kd, vd, scale=scale, causal=causal)
+    (o.float() * do.cuda().float()).sum().backward()
+    torch.cuda.synchronize()
+    got = {"dq": qd.grad.double().cpu().numpy(), "dk": kd.grad.double().cpu().numpy(),
+           "dv": vd.grad.double().cpu().numpy()}
+    check(got, oracle.attention_backward(q, k, v, do, scale, causal))
+    direct = gpu_grads(q, k, v, do, scale, causal)
+    for name in ("dk", "dv"):
+        assert np.array_equal(got[name], direct[name]), name
+    assert np.abs(got["dq"] - direct["dq"]).max() <= 1e-2 * np.abs(direct["dq"]).max()
