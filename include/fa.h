@@ -40,7 +40,7 @@ extern "C" {
 enum fa_status {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1, /* null/misaligned/overlapping pointer, bad size, bad scale */
-    FA_ERR_UNSUPPORTED = 2, /* a valid problem this build does not handle (d not 64/128) */
+    FA_ERR_UNSUPPORTED = 2, /* a valid problem the library does not handle (d not 64/128) */
     FA_ERR_NO_DEVICE = 3,   /* no CUDA device, or a pointer not on the current device */
     FA_ERR_ARCH = 4,        /* the current device is not compute capability 10.3 */
     FA_ERR_LAUNCH = 5,      /* the kernel launch itself failed (CUDA error) */
